@@ -1,0 +1,432 @@
+"""Benchmark of the DSA decode hot path on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_32k|ragged_decode|prefill_8k|indexshare_paged]
+
+A step is one pass of the whole hot path over one batch: lightning indexer -> top-k ->
+sparse MLA (for the IndexShare workload: indexer and top-k once, MLA for 4 layers).
+The default workload is the decode batch the metric is quoted on: 32 sequences x 32768
+cached tokens, one query each, Hi=64 x Di=128 fp8 indexer, k=2048, H=64, d=512 + r=64
+bf16 latent.  Inputs are synthetic (seeded, drawn on the device) and resident in HBM;
+three independent input sets rotate so that each step's ~220 MB of reads miss L2.
+
+Multi-GPU: every sequence is independent, so N ranks run N replicas on their own
+batches (weak scaling, no collective on the data path); value = all ranks' query
+tokens / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation there is) on a
+bounded sample of the same workload, on the host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode query-tokens/s at 32K ctx; achieved HBM TB/s vs B300 peak"
+UNIT = "query-tok/s"
+
+WORKLOADS = {
+    "decode_32k": "32 seq x 32768 ctx, 1 decode query each; indexer 64x128 e4m3; top-2048; "
+                  "MLA H=64 d=512 r=64 bf16",
+    "ragged_decode": "16 seq, ctx log-uniform 1024..200000 (5% planted keys), 1 decode query each",
+    "prefill_8k": "1 seq, 8192 query rows after a 57344-token prefix (65536 total)",
+    "indexshare_paged": "IndexShare group of 4 layers, 64 seq x 16384 ctx, 64-token pages",
+}
+
+
+def per_query_bytes(case):
+    """Algorithmic HBM bytes of one step, per workload: every byte the path must move once.
+
+    Indexer: the fp8 keys and their scales of every visible token, the query (q8, scale,
+    weights, position) and the written scores.  Top-k: the scores read, the indices
+    written.  Sparse MLA: the selected latent rows (d+r bf16 each), the query, the
+    indices read, the output written (and lse)."""
+    tot_idx = tot_topk = tot_mla = 0
+    D = case.d + case.r
+    for b, L in enumerate(case.lengths):
+        for i in range(case.T):
+            n = L - case.T + 1 + i
+            m = min(n, case.k)
+            tot_idx += n * (case.Di + 4) + case.Hi * case.Di + 4 + case.Hi * 4 + 4 + 4 * n
+            tot_topk += 4 * n + 4 * case.k + 4
+            tot_mla += case.layers * (m * D * 2 + case.H * D * 2 + case.H * case.d * 2 +
+                                      case.H * 4) + 4 * case.k
+    return tot_idx, tot_topk, tot_mla
+
+
+def scores_in_step(case):
+    """Bytes of the score round trip (written by the indexer, read by top-k): part of the
+    API's two-call form, not of the method, so excluded from the whole-step figure."""
+    return sum(8 * (L - case.T + 1 + i) for L in case.lengths for i in range(case.T))
+
+
+def src_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def traffic_for(kernel_files, kernel):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_sha") != src_sha(kernel_files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_workload(name, device, seed_offset=0):
+    from sparse_attention_29_b300 import inputs
+    return inputs.preset(name, seed=inputs.PRESETS[name]["seed"] + seed_offset, device=device)
+
+
+def run_reference(args, world, rank):
+    """The oracle, timed on the host's cores on a bounded sample of the workload."""
+    if rank != 0:
+        return 0
+    import oracle
+    from sparse_attention_29_b300 import inputs
+    oracle.build()
+    p = dict(inputs.PRESETS[args.workload])
+    # a bounded sample: one sequence (one query row) of the workload per step
+    if args.workload == "ragged_decode":
+        p["lengths"] = [inputs.ragged_lengths(16, 1024, 200000, p["seed"])[0]]
+    elif args.workload == "prefill_8k":
+        p["lengths"] = [65536]
+        p["T"] = 1
+    else:
+        p["lengths"] = p["lengths"][:1]
+    case = inputs.make_case(args.workload + "-sample", **p)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        if case.layers > 1:
+            oracle.indexshare_group(case)
+        else:
+            oracle.dsa_layer(case)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per_step = sum(times) / len(times)
+    value = case.rows / per_step
+    cores = oracle.num_threads()
+    sample = (f"{case.rows} query row(s) of {args.workload} per step "
+              f"(context {case.lengths[0]}, full indexer + top-k + MLA"
+              f"{' x4 layers' if case.layers > 1 else ''})")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload + ": " + WORKLOADS[args.workload]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(workload, budget_s=12.0):
+    """The oracle as it stands, on a bounded sample of the workload (rank 0, N=1)."""
+    import oracle
+    from sparse_attention_29_b300 import inputs
+    oracle.build()
+    p = dict(inputs.PRESETS[workload])
+    if workload == "ragged_decode":
+        p["lengths"] = [inputs.ragged_lengths(16, 1024, 200000, p["seed"])[0]]
+    elif workload == "prefill_8k":
+        p["T"] = 1
+    else:
+        p["lengths"] = p["lengths"][:1]
+    case = inputs.make_case(workload + "-sample", **p)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        if case.layers > 1:
+            oracle.indexshare_group(case)
+        else:
+            oracle.dsa_layer(case)
+        n += case.rows
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} query row(s) of {workload} (context {case.lengths[0]}), "
+                      f"fp64 indexer + top-k + MLA, {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--sets", type=int, default=3, help="rotating input sets")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    from sparse_attention_29_b300 import build as libbuild
+    from sparse_attention_29_b300 import capi
+    from sparse_attention_29_b300.pipeline import DsaLayer
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    libbuild.build()
+    capi.load()
+
+    # baseline CPU timing first (before the GPU is busy; host cores only)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline(args.workload)
+
+    sets = [make_workload(args.workload, dev, seed_offset=1000 * rank + 17 * i)
+            for i in range(args.sets)]
+    layers = [DsaLayer(c) for c in sets]
+    case = sets[0]
+    shared = case.layers > 1
+    stream = torch.cuda.current_stream()
+
+    def step(lay):
+        if shared:
+            lay.run_shared()
+        else:
+            lay.run()
+
+    launches_per_step = 3 + (1 if layers[0].ws_bytes else 0)
+    for i in range(args.warmup):
+        step(layers[i % len(layers)])
+    torch.cuda.synchronize()
+    layers[0].check_device_error()
+
+    # ---- timed region: K steps, per-kernel events on the launching stream -------------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            lay = layers[i % len(layers)]
+            ev[i][0].record(stream)
+            lay.indexer()
+            ev[i][1].record(stream)
+            lay.topk()
+            ev[i][2].record(stream)
+            if shared:
+                lay.mla_shared()
+            else:
+                lay.mla()
+            ev[i][3].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    t = torch.tensor([total_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    k_idx = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    k_topk = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    k_mla = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    layers[0].check_device_error()
+
+    b_idx, b_topk, b_mla = per_query_bytes(case)
+    step_bytes = b_idx + b_topk + b_mla - scores_in_step(case)
+    q_tokens = case.rows
+    value = world * q_tokens / (ms_per_step * 1e-3)
+
+    # ---- e2e: host (pinned) inputs -> C-ABI calls -> host result, every step ----------
+    e2e = None
+    if not args.no_e2e:
+        host_in = []
+        for c in sets:
+            h = {"q8": c.q8.cpu().pin_memory(), "q_scale": c.q_scale.cpu().pin_memory(),
+                 "w": c.w.cpu().pin_memory(), "q_pos": c.q_pos.cpu().pin_memory(),
+                 "q": [q.cpu().pin_memory() for q in c.q]}
+            host_in.append(h)
+        host_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in lay.out]
+                    for lay in layers]
+        host_lse = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in lay.lse]
+                    for lay in layers]
+        h2d = sum(x.numel() * x.element_size() for x in
+                  (host_in[0]["q8"], host_in[0]["q_scale"], host_in[0]["w"], host_in[0]["q_pos"]))
+        h2d += sum(q.numel() * q.element_size() for q in host_in[0]["q"])
+        d2h = sum(o.numel() * o.element_size() for o in host_out[0] + host_lse[0])
+
+        def e2e_step(i):
+            j = i % len(layers)
+            c, lay, h = sets[j], layers[j], host_in[j]
+            c.q8.copy_(h["q8"], non_blocking=True)
+            c.q_scale.copy_(h["q_scale"], non_blocking=True)
+            c.w.copy_(h["w"], non_blocking=True)
+            c.q_pos.copy_(h["q_pos"], non_blocking=True)
+            for qd, qh in zip(c.q, h["q"]):
+                qd.copy_(qh, non_blocking=True)
+            step(lay)
+            for od, oh in zip(lay.out, host_out[j]):
+                oh.copy_(od, non_blocking=True)
+            for od, oh in zip(lay.lse, host_lse[j]):
+                oh.copy_(od, non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        t2 = torch.tensor([s2.elapsed_time(e2)], device=dev)
+        if world > 1:
+            dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t2.item()) / args.steps
+        e2e = {"value": world * q_tokens / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+    idx_files = ["sparse_attention_29_b300/csrc/indexer.cu", "sparse_attention_29_b300/csrc/ptx.cuh"]
+    achieved = b_idx / (k_idx * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16 (fp32 accumulate)",
+        "data": "synthetic (seeded, drawn on device)",
+        "config": {"workload": args.workload + ": " + WORKLOADS[args.workload],
+                   "batch": case.B, "rows": case.rows, "context": case.lengths[0] if len(set(case.lengths)) == 1 else "ragged",
+                   "k": case.k, "layers": case.layers, "page_size": case.page_size,
+                   "l2": f"inputs larger than L2, {args.sets} rotating input sets",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_tbs": step_bytes / (ms_per_step * 1e-3) / 1e12,
+        "hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+        "step_bytes": step_bytes,
+        "kernel_ms": {"indexer": k_idx, "topk": k_topk, "sparse_mla": k_mla},
+        "roofline": {"bound": "hbm", "kernel": "indexer", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic_for(idx_files, "indexer"),
+                     "algorithmic_bytes": b_idx, "peak_source": peak_src},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if cpu_base:
+        line["cpu_baseline"] = cpu_base
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -4,7 +4,7 @@ lightning indexer -> causal top-k -> sparse MLA (MQA / absorbed mode), with Inde
 reuse of one index set across a group of layers and an optional paged cache.
 
 The compute lives in the C-ABI library libdsa.so (CUDA kernels, see csrc/); the Python
-module `libdsa` is a thin ctypes binding over it.  Importing this package loads nothing:
+module `capi` is a thin ctypes binding over it.  Importing this package loads nothing:
 `inputs` (seeded synthetic workloads) works without a GPU.
 """
-__all__ = ["inputs", "libdsa"]
+__all__ = ["inputs", "capi", "pipeline"]

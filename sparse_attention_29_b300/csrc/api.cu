@@ -1,0 +1,277 @@
+// api.cu -- the C ABI of libdsa: argument checks on the host, tensor-map set-up, launch.
+//
+// Every entry point validates its arguments before it launches anything and returns a
+// dsa_status_t; no C++ exception crosses the ABI.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+using namespace dsa;
+
+namespace {
+
+#define DSA_VERSION_STRING "libdsa 0.1.0 (sm_103a)"
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+dsa_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return DSA_OK;
+    (void)cudaGetLastError();
+    return DSA_ERR_CUDA;
+}
+
+int current_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool layout_ok(const dsa_cache_layout_t *L, int B, bool need_page64) {
+    if (!L || L->num_rows <= 0) return false;
+    if (L->block_table) {
+        if (L->page_size <= 0 || L->pages_per_seq <= 0) return false;
+        if (need_page64 && (L->page_size % 64) != 0) return false;
+    } else if (!L->seq_start) {
+        return false;
+    }
+    (void)B;
+    return true;
+}
+
+CacheLayout to_layout(const dsa_cache_layout_t *L) {
+    CacheLayout c;
+    c.seq_start = L->seq_start;
+    c.block_table = L->block_table;
+    c.page_size = L->page_size;
+    c.pages_per_seq = L->pages_per_seq;
+    c.num_rows = L->num_rows;
+    return c;
+}
+
+int pow2_at_least(int x) {
+    int p = 32;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int n_layers,
+                        const dsa_cache_layout_t *layout, const int32_t *idx, int B, int T,
+                        int H, int d, int r, int k, float scale, uint16_t *const *out,
+                        float *const *lse, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
+    if (!q || !kv || !out || !idx || !layout) return DSA_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || r < 0 || k <= 0) return DSA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || scale != scale) return DSA_ERR_INVALID_ARG;
+    if (H > 64 || d % 64 != 0 || d > 512 || r > 64 || (d + r) % 8 != 0 || k > 8192)
+        return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)B * T * n_layers > (int64_t)1 << 30) return DSA_ERR_UNSUPPORTED;
+    if (!layout_ok(layout, B, false)) return DSA_ERR_INVALID_ARG;
+    MlaParams p;
+    std::memset(&p, 0, sizeof p);
+    for (int g = 0; g < n_layers; ++g) {
+        if (!q[g] || !kv[g] || !out[g]) return DSA_ERR_INVALID_ARG;
+        if (!aligned16(q[g]) || !aligned16(kv[g])) return DSA_ERR_INVALID_ARG;
+        p.q[g] = q[g];
+        p.kv[g] = kv[g];
+        p.out[g] = out[g];
+        p.lse[g] = lse ? lse[g] : nullptr;
+    }
+    p.idx = idx;
+    p.layout = to_layout(layout);
+    p.layers = n_layers;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.d = d;
+    p.r = r;
+    p.k = k;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int sms = current_sm_count();
+    if (sms <= 0) return DSA_ERR_CUDA;
+    const int units = B * T * n_layers;
+    p.splits = mla_num_splits(units, k, sms);
+    const int ntiles = (k + 127) / 128;
+    p.tiles_per_split = (ntiles + p.splits - 1) / p.splits;
+    p.splits = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    const size_t need = mla_partial_bytes(units, p.splits, d);
+    if (need) {
+        if (!workspace || workspace_bytes < need) return DSA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+        p.partial = static_cast<float *>(workspace);
+    }
+    return from_cuda(launch_sparse_mla(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dsa_version(void) { return DSA_VERSION_STRING; }
+
+const char *dsa_status_string(dsa_status_t s) {
+    switch (s) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported shape";
+        case DSA_ERR_CUDA: return "CUDA error";
+        case DSA_ERR_WORKSPACE: return "workspace missing or too small";
+        case DSA_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const float *w,
+                                const uint8_t *k8_cache, const float *k_scale,
+                                const dsa_cache_layout_t *layout, const int32_t *q_pos,
+                                int B, int T, int Hi, int Di, int Lmax, float *scores,
+                                void *stream) {
+    if (!q8 || !q_scale || !w || !k8_cache || !k_scale || !q_pos || !scores)
+        return DSA_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || Hi <= 0 || Di <= 0 || Lmax <= 0) return DSA_ERR_INVALID_ARG;
+    if (Di != 32 && Di != 64 && Di != 128) return DSA_ERR_UNSUPPORTED;
+    const int HP = (Hi + 15) / 16 * 16;
+    if (HP > 256) return DSA_ERR_UNSUPPORTED;
+    if (!aligned16(q8) || !aligned16(k8_cache)) return DSA_ERR_INVALID_ARG;
+    if (!layout_ok(layout, B, true)) return DSA_ERR_INVALID_ARG;
+    if ((int64_t)layout->num_rows >= ((int64_t)1 << 31) - 256) return DSA_ERR_UNSUPPORTED;
+    IndexerParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q8 = q8;
+    p.q_scale = q_scale;
+    p.w = w;
+    p.k_scale = k_scale;
+    p.q_pos = q_pos;
+    p.scores = scores;
+    p.layout = to_layout(layout);
+    p.B = B;
+    p.T = T;
+    p.Hi = Hi;
+    p.Di = Di;
+    p.Lmax = Lmax;
+    p.HP = HP;
+    p.G = 256 / HP;
+    if (p.G > T) p.G = T;
+    if (p.G > 16) p.G = 16;
+    p.N = p.G * HP;
+    p.groups_per_seq = (T + p.G - 1) / p.G;
+    const int64_t ng = (int64_t)B * p.groups_per_seq;
+    if (ng > 16384) return DSA_ERR_UNSUPPORTED;
+    p.num_groups = (int)ng;
+    p.acc_cols = pow2_at_least(p.N);
+    p.num_acc = 512 / p.acc_cols;
+    if (p.num_acc > 4) p.num_acc = 4;
+
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_tiled();
+    if (!encode) return DSA_ERR_CUDA;
+    CUtensorMap kmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)Di, (cuuint64_t)layout->num_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)Di};
+    const cuuint32_t box[2] = {(cuuint32_t)Di, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = Di == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : Di == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUresult cr = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(k8_cache),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return DSA_ERR_CUDA;
+    const int sms = current_sm_count();
+    if (sms <= 0) return DSA_ERR_CUDA;
+    return from_cuda(launch_indexer(p, kmap, sms, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int Lmax, int k,
+                      int32_t *idx, void *stream) {
+    if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
+    if (rows <= 0 || Lmax <= 0 || k <= 0) return DSA_ERR_INVALID_ARG;
+    if (k > 8192) return DSA_ERR_UNSUPPORTED;
+    TopkParams p;
+    p.scores = scores;
+    p.q_pos = q_pos;
+    p.idx = idx;
+    p.rows = rows;
+    p.Lmax = Lmax;
+    p.k = k;
+    return from_cuda(launch_topk(p, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
+                                   const dsa_cache_layout_t *layout, const int32_t *idx,
+                                   int B, int H, int d, int r, int k, float scale,
+                                   uint16_t *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    return mla_common(&q, &kv_cache, 1, layout, idx, B, 1, H, d, r, k, scale, &out,
+                      lse ? &lse : nullptr, workspace, workspace_bytes, stream);
+}
+
+dsa_status_t dsa_sparse_mla_prefill(const uint16_t *q, const uint16_t *kv_cache,
+                                    const dsa_cache_layout_t *layout, const int32_t *idx,
+                                    int B, int T, int H, int d, int r, int k, float scale,
+                                    uint16_t *out, float *lse, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+    return mla_common(&q, &kv_cache, 1, layout, idx, B, T, H, d, r, k, scale, &out,
+                      lse ? &lse : nullptr, workspace, workspace_bytes, stream);
+}
+
+dsa_status_t dsa_sparse_mla_shared(const uint16_t *const *q_layers,
+                                   const uint16_t *const *kv_layers, int n_layers,
+                                   const dsa_cache_layout_t *layout, const int32_t *idx,
+                                   int B, int T, int H, int d, int r, int k, float scale,
+                                   uint16_t *const *out_layers, float *const *lse_layers,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    return mla_common(q_layers, kv_layers, n_layers, layout, idx, B, T, H, d, r, k, scale,
+                      out_layers, lse_layers, workspace, workspace_bytes, stream);
+}
+
+size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n_layers) {
+    if (B <= 0 || T <= 0 || k <= 0) return (size_t)-1;
+    if (op == DSA_OP_INDEXER || op == DSA_OP_TOPK) return 0;
+    if (op != DSA_OP_SPARSE_MLA) return (size_t)-1;
+    if (H <= 0 || H > 64 || d <= 0 || d % 64 != 0 || n_layers < 1 || n_layers > kMaxLayers)
+        return (size_t)-1;
+    const int sms = current_sm_count();
+    if (sms <= 0) return (size_t)-1;
+    const int units = B * T * n_layers;
+    int splits = mla_num_splits(units, k, sms);
+    const int ntiles = (k + 127) / 128;
+    const int tps = (ntiles + splits - 1) / splits;
+    splits = (ntiles + tps - 1) / tps;
+    return mla_partial_bytes(units, splits, d);
+}
+
+dsa_status_t dsa_device_error(void *stream, uint32_t *code) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return from_cuda(cudaErrorUnknown);
+    const uint32_t words[3] = {take_error_indexer(), take_error_topk(), take_error_mla()};
+    uint32_t first = 0;
+    for (uint32_t v : words) {
+        if (v == 0xFFFFFFFFu) return DSA_ERR_CUDA;
+        if (v && !first) first = v;
+    }
+    if (code) *code = first;
+    return first ? DSA_ERR_DEVICE : DSA_OK;
+}
+
+}  // extern "C"

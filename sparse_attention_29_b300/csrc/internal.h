@@ -1,0 +1,82 @@
+// internal.h -- launch parameters shared by the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Read and clear the device error word of each kernel file (0: no error;
+// 0xFFFFFFFF: the read itself failed).
+uint32_t take_error_indexer();
+uint32_t take_error_topk();
+uint32_t take_error_mla();
+
+// How token s of sequence b maps to a physical cache row (see dsa_cache_layout_t).
+struct CacheLayout {
+    const int32_t *seq_start;
+    const int32_t *block_table;
+    int32_t page_size;
+    int32_t pages_per_seq;
+    int64_t num_rows;
+};
+
+// ---- lightning indexer ------------------------------------------------------------
+struct IndexerParams {
+    const uint8_t *q8;
+    const float *q_scale;
+    const float *w;
+    const float *k_scale;
+    const int32_t *q_pos;
+    float *scores;
+    CacheLayout layout;
+    int B, T, Hi, Di, Lmax;
+    int HP;        // heads per query padded to a multiple of 16
+    int G;         // query rows per tensor-core group (N = G * HP)
+    int N;         // MMA N
+    int groups_per_seq;
+    int num_groups;
+    int acc_cols;  // TMEM columns per accumulator buffer
+    int num_acc;   // accumulator buffers
+    int stages;    // key pipeline depth
+};
+
+cudaError_t launch_indexer(const IndexerParams &p, const CUtensorMap &kmap, int num_sms,
+                           cudaStream_t stream);
+
+// ---- top-k ------------------------------------------------------------------------
+struct TopkParams {
+    const float *scores;
+    const int32_t *q_pos;
+    int32_t *idx;
+    int rows, Lmax, k;
+};
+
+cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream);
+
+// ---- sparse MLA -------------------------------------------------------------------
+constexpr int kMaxLayers = 8;
+
+struct MlaParams {
+    const uint16_t *q[kMaxLayers];
+    const uint16_t *kv[kMaxLayers];
+    uint16_t *out[kMaxLayers];
+    float *lse[kMaxLayers];
+    const int32_t *idx;
+    CacheLayout layout;
+    float *partial;    // split-KV partials (workspace), or nullptr when splits == 1
+    int layers, B, T, H, d, r, k;
+    float scale_log2;  // softmax scale * log2(e)
+    int splits;        // key splits per (row, layer)
+    int tiles_per_split;
+};
+
+int mla_num_splits(int rows_times_layers, int k, int num_sms);
+size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
+cudaError_t launch_sparse_mla(const MlaParams &p, cudaStream_t stream);
+
+}  // namespace dsa

@@ -1,0 +1,87 @@
+"""The C-ABI library builds, loads and exports every declared symbol; argument checks
+return their status codes without touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_29_b300 import build, capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return capi.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_symbols() == sorted(capi.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert capi.version().startswith("libdsa")
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.dsa_status_string(code)
+    assert lib.dsa_status_string(99) == b"unknown status"
+
+
+def test_null_and_range_checks_fail_before_any_launch(lib):
+    L = capi.CacheLayout(None, None, 0, 0, 0)
+    INVALID, UNSUPPORTED = 1, 2
+    # indexer: null pointers, zero sizes, unsupported head dim
+    assert lib.dsa_indexer_scores(None, None, None, None, None, ctypes.byref(L), None,
+                                  1, 1, 64, 128, 16, None, None) == INVALID
+    p = 0x1000  # never dereferenced: the checks below fail first
+    assert lib.dsa_indexer_scores(p, p, p, p, p, ctypes.byref(L), p, 0, 1, 64, 128, 16, p,
+                                  None) == INVALID
+    assert lib.dsa_indexer_scores(p, p, p, p, p, ctypes.byref(L), p, 1, 1, 64, 96, 16, p,
+                                  None) == UNSUPPORTED
+    # a layout with neither seq_start nor block table
+    assert lib.dsa_indexer_scores(p, p, p, p, p, ctypes.byref(L), p, 1, 1, 64, 128, 16, p,
+                                  None) == INVALID
+    # misaligned key cache
+    L2 = capi.CacheLayout(p, None, 0, 0, 100)
+    assert lib.dsa_indexer_scores(p, p, p, p + 4, p, ctypes.byref(L2), p, 1, 1, 64, 128, 16,
+                                  p, None) == INVALID
+    # paged indexer needs page_size % 64 == 0
+    L3 = capi.CacheLayout(None, p, 32, 4, 128)
+    assert lib.dsa_indexer_scores(p, p, p, p, p, ctypes.byref(L3), p, 1, 1, 64, 128, 16, p,
+                                  None) == INVALID
+    # top-k: k out of range
+    assert lib.dsa_topk(p, p, 4, 100, 0, p, None) == INVALID
+    assert lib.dsa_topk(p, p, 4, 100, 9000, p, None) == UNSUPPORTED
+    assert lib.dsa_topk(None, p, 4, 100, 64, p, None) == INVALID
+    # sparse MLA: shapes outside the build
+    assert lib.dsa_sparse_mla_decode(p, p, ctypes.byref(L2), p, 1, 128, 512, 64, 2048,
+                                     ctypes.c_float(0.0625), p, None, None, 0,
+                                     None) == UNSUPPORTED
+    assert lib.dsa_sparse_mla_decode(p, p, ctypes.byref(L2), p, 1, 64, 500, 64, 2048,
+                                     ctypes.c_float(0.0625), p, None, None, 0,
+                                     None) == UNSUPPORTED
+    assert lib.dsa_sparse_mla_decode(p, p, ctypes.byref(L2), p, 1, 64, 512, 64, 2048,
+                                     ctypes.c_float(-1.0), p, None, None, 0, None) == INVALID
+    assert lib.dsa_sparse_mla_decode(p + 8, p, ctypes.byref(L2), p, 1, 64, 512, 64, 2048,
+                                     ctypes.c_float(0.0625), p, None, None, 0,
+                                     None) == INVALID
+    assert lib.dsa_sparse_mla_shared(None, None, 0, ctypes.byref(L2), p, 1, 1, 64, 512, 64,
+                                     2048, ctypes.c_float(0.0625), None, None, None, 0,
+                                     None) == INVALID
+
+
+def test_workspace_query_without_gpu(lib):
+    assert lib.dsa_workspace_bytes(0, 1, 1, 64, 512, 2048, 1) == 0
+    assert lib.dsa_workspace_bytes(1, 1, 1, 64, 512, 2048, 1) == 0
+    assert lib.dsa_workspace_bytes(2, 0, 1, 64, 512, 2048, 1) == ctypes.c_size_t(-1).value

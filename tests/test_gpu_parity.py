@@ -1,0 +1,223 @@
+"""GPU parity: libdsa's CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases span several 128-key tiles with ragged tails; the integer-valued workload is
+checked bit-exactly.  Tolerances are defined in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import (check_mla, check_mla_integer, check_scores, check_topk_sets, cpu,
+                    subcase)
+from sparse_attention_29_b300 import build, capi, inputs
+from sparse_attention_29_b300.pipeline import DsaLayer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    capi.load()
+    assert torch.cuda.is_available()
+
+
+def gpu_layer(case):
+    return DsaLayer(case.to("cuda"))
+
+
+def assert_no_device_error(layer):
+    layer.check_device_error()
+
+
+# ---- integer-valued workload: exact -------------------------------------------------------
+
+def test_tiny_int_exact():
+    case = inputs.preset("tiny_int")
+    lay = gpu_layer(case)
+    lay.run()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref_scores = oracle.indexer_scores(case)
+    g = cpu(lay.scores).double().numpy()
+    vis = np.arange(case.Lmax)[None, :] <= case.q_pos.numpy()[:, None]
+    assert np.array_equal(g[vis], ref_scores[vis])          # bit-exact scores
+    ref_idx = oracle.topk(ref_scores, case.q_pos, case.k)
+    assert np.array_equal(cpu(lay.idx).numpy(), ref_idx)     # bit-exact indices (with ties)
+    ref_out, ref_lse = oracle.sparse_mla(case, ref_idx)
+    check_mla_integer(lay.out[0], case, lay.idx, ref_out)
+    gl = cpu(lay.lse[0]).double().numpy()
+    assert np.max(np.abs(gl - ref_lse)) <= 2.5e-3
+
+
+# ---- indexer ------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("lengths,T,paged", [
+    ([3000, 700, 2048 + 131, 77], 1, 0),     # decode, ragged, one context under one tile
+    ([2500], 37, 0),                         # prefill form, ragged row group
+    ([1500, 900], 5, 64),                    # prefill form on a paged cache
+    ([4100, 129, 2048], 1, 64),              # decode on a paged cache
+])
+def test_indexer_matches_oracle(lengths, T, paged):
+    case = inputs.make_case(seed=101 + T, lengths=lengths, T=T, page_size=paged)
+    lay = gpu_layer(case)
+    lay.indexer()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref = oracle.indexer_scores(case)
+    check_scores(lay.scores, ref, case.q_pos)
+
+
+@pytest.mark.parametrize("Hi,Di", [(4, 32), (16, 64), (24, 128), (64, 32)])
+def test_indexer_head_shapes(Hi, Di):
+    case = inputs.make_case(seed=7 + Hi, lengths=[1000, 301], T=3, Hi=Hi, Di=Di, H=4, d=64,
+                            r=16, k=256)
+    lay = gpu_layer(case)
+    lay.indexer()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    check_scores(lay.scores, oracle.indexer_scores(case), case.q_pos)
+
+
+# ---- top-k on fixed fp32 scores (bit-exact; both sides compare fp32 values) -----------------
+
+def _scores_with_ties(rows, Lmax, seed, levels=None):
+    g = torch.Generator().manual_seed(seed)
+    if levels:
+        return (torch.randint(0, levels, (rows, Lmax), generator=g).float() * 0.5 - 3.0)
+    return torch.randn((rows, Lmax), generator=g)
+
+
+@pytest.mark.parametrize("Lmax,k,levels", [
+    (3000, 2048, None), (3000, 2048, 7), (40960, 2048, None), (41000, 2048, 13),
+    (65536, 2048, None), (200000, 2048, None), (5000, 100, 3), (9000, 8192, None),
+    (1000, 1, None), (70000, 2048, 1),
+])
+def test_topk_exact_on_fixed_scores(Lmax, k, levels):
+    rows = 6
+    s = _scores_with_ties(rows, Lmax, seed=Lmax + k, levels=levels)
+    # positions: dense (n <= k), exactly k, k + 1, and long rows
+    q_pos = torch.tensor([min(k - 1, Lmax - 1), min(k, Lmax - 1), Lmax - 1, Lmax // 2,
+                          max(0, Lmax - 3), Lmax - 1], dtype=torch.int32)
+    if levels is None:
+        s[5, : Lmax // 3] = 0.0                    # a run of exact zeros
+        s[5, 7] = -0.0
+    out = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    capi.dsa_topk(s.cuda(), q_pos.cuda(), rows, Lmax, k, out)
+    torch.cuda.synchronize()
+    ref = oracle.topk(s.numpy(), q_pos.numpy(), k)
+    assert np.array_equal(cpu(out).numpy(), ref)
+
+
+# ---- sparse MLA ---------------------------------------------------------------------------
+
+def _random_idx(case, seed, frac_invalid=0.0):
+    g = np.random.default_rng(seed)
+    rows = case.rows
+    idx = np.full((rows, case.k), -1, np.int32)
+    for t in range(rows):
+        n = int(case.q_pos[t]) + 1
+        m = min(n, case.k)
+        sel = np.sort(g.choice(n, size=m, replace=False))
+        idx[t, :m] = sel
+        if frac_invalid:
+            kill = g.random(case.k) < frac_invalid
+            idx[t, kill] = -1
+    return torch.from_numpy(idx)
+
+
+@pytest.mark.parametrize("lengths,T,k,paged", [
+    ([5000, 3000, 2100], 1, 2048, 0),   # decode: few rows -> split-KV path
+    ([700, 300], 1, 2048, 0),           # dense rows (fewer tokens than k), -1 padding
+    ([1200], 24, 512, 0),               # prefill form
+    ([2600, 1900], 1, 1000, 64),        # paged, k not a multiple of the tile
+])
+def test_sparse_mla_matches_oracle(lengths, T, k, paged):
+    case = inputs.make_case(seed=200 + k, lengths=lengths, T=T, k=k, page_size=paged)
+    lay = gpu_layer(case)
+    idx = _random_idx(case, seed=k, frac_invalid=0.02)
+    lay.mla(idx=idx.cuda())
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref_out, ref_lse = oracle.sparse_mla(case, idx)
+    check_mla(lay.out[0], lay.lse[0], ref_out, ref_lse)
+
+
+def test_sparse_mla_small_heads_and_dims():
+    case = inputs.make_case(seed=9, lengths=[900, 400], T=2, Hi=4, Di=32, H=12, d=128, r=32,
+                            k=300, softmax_scale=0.1)
+    lay = gpu_layer(case)
+    idx = _random_idx(case, seed=3)
+    lay.mla(idx=idx.cuda())
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.sparse_mla(case, idx)
+    check_mla(lay.out[0], lay.lse[0], ref_out, ref_lse)
+
+
+def test_sparse_mla_all_invalid_row():
+    case = inputs.make_case(seed=10, lengths=[500, 600], T=1, k=256)
+    lay = gpu_layer(case)
+    idx = _random_idx(case, seed=4)
+    idx[1] = -1
+    lay.mla(idx=idx.cuda())
+    torch.cuda.synchronize()
+    out = cpu(lay.out[0]).float()
+    assert torch.all(out[1] == 0)
+    assert torch.all(torch.isneginf(cpu(lay.lse[0])[1]))
+    ref_out, ref_lse = oracle.sparse_mla(case, idx)
+    check_mla(lay.out[0][:1], lay.lse[0][:1], ref_out[:1], ref_lse[:1])
+
+
+# ---- whole layer and IndexShare ------------------------------------------------------------
+
+@pytest.mark.parametrize("lengths,T,paged", [
+    ([6000, 1000, 2049], 1, 0),
+    ([3000], 16, 0),
+])
+def test_dsa_layer_end_to_end(lengths, T, paged):
+    case = inputs.make_case(kind="planted", seed=300 + T, lengths=lengths, T=T,
+                            page_size=paged)
+    lay = gpu_layer(case)
+    lay.run()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref_scores = oracle.indexer_scores(case)
+    check_scores(lay.scores, ref_scores, case.q_pos)
+    check_topk_sets(lay.idx, ref_scores, case.q_pos, case.k)
+    ref_out, ref_lse = oracle.sparse_mla(case, cpu(lay.idx))
+    check_mla(lay.out[0], lay.lse[0], ref_out, ref_lse)
+
+
+def test_indexshare_paged_group():
+    case = inputs.make_case(seed=400, lengths=[3000, 2200, 700], T=1, layers=4, page_size=64)
+    lay = gpu_layer(case)
+    lay.run_shared()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref_idx, per_layer = oracle.indexshare_group(case)
+    ref_scores = oracle.indexer_scores(case)
+    check_topk_sets(lay.idx, ref_scores, case.q_pos, case.k)
+    gidx = cpu(lay.idx)
+    for g in range(4):
+        ref_out, ref_lse = oracle.sparse_mla(case, gidx, layer=g)
+        check_mla(lay.out[g], lay.lse[g], ref_out, ref_lse)
+    # paged == contiguous on the un-paged copy, bit for bit
+    flat = gpu_layer(inputs.unpage(case))
+    flat.run_shared()
+    torch.cuda.synchronize()
+    assert torch.equal(flat.idx, lay.idx)
+    for g in range(4):
+        assert torch.equal(flat.out[g], lay.out[g])
+
+
+def test_shared_equals_separate_layer_calls():
+    case = inputs.make_case(seed=401, lengths=[2500, 4000], T=1, layers=3)
+    lay = gpu_layer(case)
+    lay.run_shared()
+    shared = [o.clone() for o in lay.out]
+    for g in range(3):
+        lay.mla(layer=g)
+    torch.cuda.synchronize()
+    for g in range(3):
+        assert torch.equal(shared[g], lay.out[g])
