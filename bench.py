@@ -100,32 +100,29 @@ def traffic_for(kernel_files, kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms into a file while the
+    block runs (a load pre-roll plus the timed region)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        fd, self.path = tempfile.mkstemp(prefix="dsa_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except (OSError, FileNotFoundError):
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
             self.proc = None
         return self
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
 
     def __exit__(self, *a):
         if self.proc:
@@ -138,7 +135,13 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        try:
+            with open(self.path) as f:
+                lines = f.read().splitlines()
+            os.unlink(self.path)
+        except OSError:
+            lines = []
+        for ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -153,7 +156,8 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "1 s load pre-roll + timed region"}
 
 
 def dist_setup():
@@ -305,6 +309,14 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # untimed pre-roll of the same steps, so that the clock samples see this load
+        t_stop, i = time.time() + 1.0, 0
+        while time.time() < t_stop:
+            step(layers[i % len(layers)])
+            i += 1
+            if i % 16 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
             lay = layers[i % len(layers)]

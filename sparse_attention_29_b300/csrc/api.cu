@@ -87,12 +87,14 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
     if (H > 64 || d % 64 != 0 || d > 512 || r > 64 || (d + r) % 8 != 0 || k > 8192)
         return DSA_ERR_UNSUPPORTED;
     if ((int64_t)B * T * n_layers > (int64_t)1 << 30) return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)B * T * H >= ((int64_t)1 << 31) - 64) return DSA_ERR_UNSUPPORTED;
+    if (layout && layout->num_rows >= ((int64_t)1 << 31) - 64) return DSA_ERR_UNSUPPORTED;
     if (!layout_ok(layout, B, false)) return DSA_ERR_INVALID_ARG;
     MlaParams p;
     std::memset(&p, 0, sizeof p);
     for (int g = 0; g < n_layers; ++g) {
         if (!q[g] || !kv[g] || !out[g]) return DSA_ERR_INVALID_ARG;
-        if (!aligned16(q[g]) || !aligned16(kv[g])) return DSA_ERR_INVALID_ARG;
+        if (!aligned16(q[g]) || !aligned16(kv[g]) || !aligned16(out[g])) return DSA_ERR_INVALID_ARG;
         p.q[g] = q[g];
         p.kv[g] = kv[g];
         p.out[g] = out[g];
@@ -121,7 +123,31 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
         if (!aligned16(workspace)) return DSA_ERR_INVALID_ARG;
         p.partial = static_cast<float *>(workspace);
     }
-    return from_cuda(launch_sparse_mla(p, static_cast<cudaStream_t>(stream)));
+    // TMA descriptors: q as [rows*H, D] (64-row x 64-column boxes), kv as [num_rows, D]
+    // (one-row boxes for gather4), bf16, 128-byte swizzle
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_tiled();
+    if (!encode) return DSA_ERR_CUDA;
+    MlaMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    const int D = d + r;
+    for (int g = 0; g < n_layers; ++g) {
+        const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)B * T * H};
+        const cuuint64_t kdims[2] = {(cuuint64_t)D, (cuuint64_t)layout->num_rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        const cuuint32_t qbox[2] = {64, 64};
+        const cuuint32_t kbox[2] = {64, 1};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult c1 = encode(&maps.q[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                             const_cast<uint16_t *>(q[g]), qdims, strides, qbox, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult c2 = encode(&maps.kv[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                             const_cast<uint16_t *>(kv[g]), kdims, strides, kbox, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (c1 != CUDA_SUCCESS || c2 != CUDA_SUCCESS) return DSA_ERR_CUDA;
+    }
+    return from_cuda(launch_sparse_mla(p, maps, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

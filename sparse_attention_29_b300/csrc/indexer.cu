@@ -354,10 +354,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int key_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        // this thread's key scale for the tile at cursor c (0 if the row is invalid); the
+        // loads run two tiles ahead of their use, off the critical path
+        auto key_scale = [&](const TileCursor &c) -> float {
+            if (!c.valid()) return 0.f;
+            const int bb = c.g / p.groups_per_seq;
+            const int s = c.j * kTileKeys + key_in_tile;
+            int64_t row;
+            if (p.layout.block_table) {
+                const int lp = s / p.layout.page_size;
+                if (lp >= p.layout.pages_per_seq) return 0.f;
+                const int page = p.layout.block_table[(int64_t)bb * p.layout.pages_per_seq + lp];
+                if (page < 0) return 0.f;
+                row = (int64_t)page * p.layout.page_size + s % p.layout.page_size;
+            } else {
+                row = (int64_t)p.layout.seq_start[bb] + s;
+            }
+            return (row >= 0 && row < p.layout.num_rows) ? __ldg(p.k_scale + row) : 0.f;
+        };
         TileCursor cur;
         cur.init(prefix, p.num_groups, tb, te);
+        TileCursor ahead = cur;
+        float ksc_ring0 = key_scale(ahead);
+        ahead.next();
+        float ksc_ring1 = key_scale(ahead);
+        ahead.next();
         int it = 0, gcount = 0, slot = 0;
         for (; cur.valid(); cur.next(), ++it) {
+            const float ksc = ksc_ring0;
+            ksc_ring0 = ksc_ring1;
+            ksc_ring1 = key_scale(ahead);
+            ahead.next();
             const int b = cur.g / p.groups_per_seq;
             if (cur.first_in_range(tb)) {
                 slot = gcount & 1;
@@ -374,28 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nr = min(p.G, p.T - gi * p.G);
             const int s = cur.j * kTileKeys + key_in_tile;
             const int *pos = gpos + slot * 16;
-            int maxpos = -1;
-            for (int qi = 0; qi < nr; ++qi) maxpos = max(maxpos, pos[qi]);
-            float ksc = 0.f;
-            if (s <= maxpos) {
-                bool bad = false;
-                int64_t row;
-                if (p.layout.block_table) {
-                    const int lp = s / p.layout.page_size;
-                    const int page = lp < p.layout.pages_per_seq
-                        ? p.layout.block_table[(int64_t)b * p.layout.pages_per_seq + lp] : -1;
-                    row = (int64_t)page * p.layout.page_size + s % p.layout.page_size;
-                    bad = page < 0;
-                } else {
-                    row = (int64_t)p.layout.seq_start[b] + s;
-                }
-                bad = bad || row < 0 || row >= p.layout.num_rows;
-                ksc = bad ? 0.f : p.k_scale[row];
-            }
             const float *wq = wbuf + slot * p.N;
             const uint32_t tacc = tmem + lane_addr + (uint32_t)(abuf * p.acc_cols);
             for (int qi = 0; qi < nr; ++qi) {
-                float acc = 0.f;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
                 for (int c0 = 0; c0 < p.HP; c0 += 64) {
                     uint32_t v[4][16];
                     const int nchunk = min(4, (p.HP - c0) / 16);
@@ -410,15 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e4 = 0; e4 < 4; ++e4) {
                                 const float4 ww = w4[e4];
-                                acc = fmaf(ww.x, fmaxf(__uint_as_float(v[c][e4 * 4 + 0]), 0.f), acc);
-                                acc = fmaf(ww.y, fmaxf(__uint_as_float(v[c][e4 * 4 + 1]), 0.f), acc);
-                                acc = fmaf(ww.z, fmaxf(__uint_as_float(v[c][e4 * 4 + 2]), 0.f), acc);
-                                acc = fmaf(ww.w, fmaxf(__uint_as_float(v[c][e4 * 4 + 3]), 0.f), acc);
+                                a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[c][e4 * 4 + 0]), 0.f), a0);
+                                a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[c][e4 * 4 + 1]), 0.f), a1);
+                                a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[c][e4 * 4 + 2]), 0.f), a2);
+                                a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[c][e4 * 4 + 3]), 0.f), a3);
                             }
                         }
                     }
                 }
-                if (s <= pos[qi]) p.scores[(int64_t)(r0 + qi) * p.Lmax + s] = acc * ksc;
+                if (s <= pos[qi])
+                    p.scores[(int64_t)(r0 + qi) * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
             }
             tc_fence_before();
             __syncwarp();

@@ -75,8 +75,14 @@ struct MlaParams {
     int tiles_per_split;
 };
 
+// TMA descriptors of every layer: q viewed as [rows*H, d+r], kv as [num_rows, d+r] (bf16)
+struct MlaMaps {
+    CUtensorMap q[kMaxLayers];
+    CUtensorMap kv[kMaxLayers];
+};
+
 int mla_num_splits(int rows_times_layers, int k, int num_sms);
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
-cudaError_t launch_sparse_mla(const MlaParams &p, cudaStream_t stream);
+cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);
 
 }  // namespace dsa

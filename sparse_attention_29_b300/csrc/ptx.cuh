@@ -133,6 +133,27 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// Gather four rows (y0..y3) of a 2D tensor, each `box width` elements wide starting at
+// column x, into four consecutive box rows in shared memory.  The tensor map's box must be
+// one row high.  x must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_gather4(void *smem_dst, const CUtensorMap *map,
+                                            uint64_t *bar, int x, int y0, int y1, int y2,
+                                            int y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1),
+        "r"(y2), "r"(y3)
+        : "memory");
+}
+
+// Add `bytes` to the barrier's expected transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared; src_bytes < 16 zero-fills the rest
 // (src_bytes == 0 reads nothing).
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src,

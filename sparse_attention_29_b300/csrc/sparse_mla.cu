@@ -7,9 +7,10 @@
 //     logit[h, j] = scale * q[h, :] . c_j          (key = the whole row)
 //     o[h, :]     = sum_j softmax_j(logit[h, :]) c_j[:d]   (value = the latent part)
 //
-// Mapping onto sm_103a.  The selected rows are gathered 128 at a time (cp.async, 16-byte
-// granules) into shared memory in the tensor cores' 128-byte-swizzled layout: chunk c of
-// a tile holds dims 64c..64c+63 of the 128 rows.  That one layout serves both products:
+// Mapping onto sm_103a.  The selected rows are gathered 128 at a time by TMA
+// (tile::gather4: four rows x 128 bytes per instruction) into shared memory in the tensor
+// cores' 128-byte-swizzled layout: chunk c of a tile holds dims 64c..64c+63 of the 128
+// rows.  That one layout serves both products:
 //   S^T[key, head]  = C[key, :] . Q[head, :]      A = C (K-major), B = Q (K-major)
 //   O^T[dim, head] += C[key, dim]^T P^T[key, head] A = C^T (MN-major), B = P^T (MN-major)
 // so both run as M = 128 tcgen05 MMAs (keys resp. latent dims on M, the 64 heads on N)
@@ -24,7 +25,7 @@
 // soon as the O product that reads them has completed.
 //
 // Rows with few keys are split over several CTAs (split-KV); each writes unnormalised
-// partial results that a small combine kernel merges with the log-sum-exp rule.
+// partial results that a combine kernel merges with the log-sum-exp rule.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -33,10 +34,10 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 224;      // warps 0-3 softmax/epilogue, 4 MMA, 5-6 gather
+constexpr int kThreads = 192;      // warps 0-3 softmax/epilogue, 4 MMA, 5 TMA producer
 constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerThreads = 64;
 constexpr int kMmaWarp = 4;
+constexpr int kProducerWarp = 5;
 constexpr int kTileKeys = 128;
 constexpr int kHeads = 64;         // heads padded to 64 (N of both products)
 constexpr int kChunkBytes = kTileKeys * 128;  // 64 dims x 128 keys x 2 B
@@ -44,7 +45,7 @@ constexpr int kQChunkBytes = kHeads * 128;    // 64 dims x 64 heads x 2 B
 constexpr float kRescaleLog2 = 8.f;           // lazy rescale threshold (log2 units)
 
 struct MlaSmem {
-    uint32_t q, tile, rowaddr, red, rn, alpha, lsum, bars, total;
+    uint32_t q, tile, rows, red, rn, alpha, lsum, bars, total;
 };
 
 __host__ __device__ inline MlaSmem mla_smem(int nch) {
@@ -54,8 +55,8 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     off += (uint32_t)nch * kQChunkBytes;
     s.tile = off;
     off += (uint32_t)nch * kChunkBytes;
-    s.rowaddr = off;
-    off += kTileKeys * 8;
+    s.rows = off;
+    off += 2 * kTileKeys * 4;
     s.red = off;
     off += 4 * kHeads * 4;
     s.rn = off;
@@ -65,7 +66,7 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     s.lsum = off;
     off += kHeads * 4;
     s.bars = off;
-    off += 16 * 8 + 16;
+    off += 20 * 8 + 16;
     s.total = off;
     return s;
 }
@@ -118,7 +119,8 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
     tmem_ld_wait();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_kernel(const __grid_constant__ MlaMaps maps, const MlaParams p) {
     const int nv = p.d / 64;             // latent (value) chunks
     const int nch = nv + 1;              // + the rope chunk
     const int nmb = (nv + 1) / 2;        // M-blocks of the O product (128 dims each)
@@ -131,20 +133,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
     uint8_t *qs = smem + L.q;
     uint8_t *tile = smem + L.tile;
     uint8_t *pslot = tile + rope * kChunkBytes;
-    int64_t *rowaddr = (int64_t *)(smem + L.rowaddr);
+    int32_t *rows_sm = (int32_t *)(smem + L.rows);   // [2][128] physical rows, -1 invalid
     float *red = (float *)(smem + L.red);
     float *rn = (float *)(smem + L.rn);
     float *alpha = (float *)(smem + L.alpha);
     float *lsum = (float *)(smem + L.lsum);
     uint64_t *bars = (uint64_t *)(smem + L.bars);
-    uint64_t *full = bars;           // [ngroups]
-    uint64_t *freeb = bars + 5;      // [ngroups]
-    uint64_t *s_full = bars + 10;
-    uint64_t *p_ready = bars + 11;
-    uint64_t *o_done = bars + 12;
+    uint64_t *full = bars;           // [ngroups] chunk groups landed
+    uint64_t *freeb = bars + 5;      // [ngroups] chunk groups free again
+    uint64_t *s_full = bars + 10;    // S^T of the tile is in TMEM
+    uint64_t *p_ready = bars + 11;   // P^T written (and O rescaled)
+    uint64_t *o_done = bars + 12;    // O^T product of the tile complete
     uint64_t *drain = bars + 13;
-    volatile int *abort_flag = (volatile int *)(bars + 16);
-    uint32_t *tmem_base_sm = (uint32_t *)(bars + 16) + 1;
+    uint64_t *q_full = bars + 14;
+    uint64_t *addr_ready = bars + 15;  // [2] row table of a tile written
+    volatile int *abort_flag = (volatile int *)(bars + 20);
+    uint32_t *tmem_base_sm = (uint32_t *)(bars + 20) + 1;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -162,40 +166,30 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
     const int t_end = min(t_begin + p.tiles_per_split, ntiles_all);
     const int ntiles = max(0, t_end - t_begin);
     const int32_t *idx_row = p.idx + (int64_t)row * p.k;
-    const uint16_t *kv = p.kv[layer];
-    const int D = p.d + p.r;
 
-    // ---- query -> shared memory (zero-padded to 64 heads and to the rope chunk) -------
-    {
-        const uint16_t *q = p.q[layer] + (int64_t)row * p.H * D;
-        for (int e = tid; e < kHeads * nch * 8; e += kThreads) {
-            const int c = e / (kHeads * 8);
-            const int rem = e - c * (kHeads * 8);
-            const int h = rem >> 3, gr = rem & 7;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (h < p.H) {
-                int col = -1;
-                if (c < nv) col = c * 64 + gr * 8;
-                else if (gr * 8 < p.r) col = p.d + gr * 8;
-                if (col >= 0) v = *(const uint4 *)(q + (int64_t)h * D + col);
-            }
-            *(uint4 *)(qs + c * kQChunkBytes + swz128(h, gr)) = v;
-        }
-        if (tid < kHeads) {
-            rn[tid] = -INFINITY;
-            alpha[tid] = 1.f;
-        }
+    if (tid < kHeads) {
+        rn[tid] = -INFINITY;
+        alpha[tid] = 1.f;
+    }
+    if (p.r < 64) {
+        // columns past d + r of the rope chunk: keep them zero in case the copy leaves
+        // out-of-range columns untouched
+        for (int e = tid; e < kTileKeys * 8; e += kThreads)
+            *(uint4 *)(tile + rope * kChunkBytes + e * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async();
     }
     if (tid == 0) {
         for (int g = 0; g < ngroups; ++g) {
-            mbar_init(&full[g], kProducerThreads);
+            mbar_init(&full[g], 32);
             mbar_init(&freeb[g], 1);
         }
         mbar_init(s_full, 1);
         mbar_init(p_ready, kSoftmaxThreads);
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
+        mbar_init(q_full, 1);
+        mbar_init(&addr_ready[0], 32);
+        mbar_init(&addr_ready[1], 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -212,28 +206,43 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
     const uint32_t tS = tmem;          // 64 columns
     const uint32_t tO = tmem + 64;     // nmb x 64 columns
 
-    if (warp >= 5) {
-        // ================= gather (2 warps; warp w owns tile rows 64w .. 64w+63) =======
-        const int pw = warp - 5;
-        const int row0 = pw * 64;
+    if (warp == kProducerWarp) {
+        // ================= TMA producer (lane l owns tile rows 4l .. 4l+3) ==============
+        const CUtensorMap *qmap = &maps.q[layer];
+        const CUtensorMap *kvmap = &maps.kv[layer];
+        if (lane == 0) {
+            prefetch_tmap(qmap);
+            prefetch_tmap(kvmap);
+            mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
+            for (int c = 0; c < nch; ++c)
+                tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
+        }
         bool ok = true;
         for (int li = 0; li < ntiles && ok; ++li) {
-            const int tile_idx = t_begin + li;
-            // element offsets of this warp's rows, -1 for padding / invalid entries
-            for (int kk = row0 + lane; kk < row0 + 64; kk += 32) {
-                const int j = tile_idx * kTileKeys + kk;
-                int64_t a = -1;
+            const int buf = li & 1;
+            const int j0 = (t_begin + li) * kTileKeys + lane * 4;
+            int y[4];
+            int first_valid = -1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0 + e;
+                int64_t r = -1;
                 if (j < p.k) {
                     const int s = idx_row[j];
                     if (s >= 0) {
-                        const int64_t r = resolve_row(p.layout, b, s);
+                        r = resolve_row(p.layout, b, s);
                         if (r < 0) record_error(KID_MLA, ERR_BAD_INDEX);
-                        else a = r * D;
                     }
                 }
-                rowaddr[kk] = a;
+                y[e] = (int)r;
+                if (r >= 0 && first_valid < 0) first_valid = (int)r;
             }
-            __syncwarp();
+            *(int4 *)(rows_sm + buf * kTileKeys + lane * 4) = make_int4(y[0], y[1], y[2], y[3]);
+            mbar_arrive(&addr_ready[buf]);
+            const bool any = first_valid >= 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (y[e] < 0) y[e] = first_valid;  // masked later; never out of range
             for (int g = 0; g < ngroups; ++g) {
                 if (li > 0) {
                     ok = mbar_wait(&freeb[g], (li - 1) & 1, KID_MLA, abort_flag);
@@ -243,45 +252,40 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
                 const bool is_rope = (g == ngroups - 1);
                 const int c0 = is_rope ? rope : 2 * g;
                 const int nck = is_rope ? 1 : min(2, nv - 2 * g);
-                const int gpr = nck * 8;  // granules per row in this group
-                for (int e = lane; e < 64 * gpr; e += 32) {
-                    const int kr = row0 + e / gpr;
-                    const int gg = e % gpr;
-                    const int c = c0 + (gg >> 3), gr = gg & 7;
-                    const int64_t a = rowaddr[kr];
-                    int col;
-                    uint32_t bytes = 16;
-                    if (is_rope) {
-                        col = p.d + gr * 8;
-                        if (gr * 8 >= p.r) bytes = 0;
+                const uint32_t lane_bytes = any ? (uint32_t)(nck * 4 * 128) : 0u;
+                uint32_t tot = __reduce_add_sync(0xffffffffu, lane_bytes);
+                if (lane == 0) mbar_expect_tx(&full[g], tot);
+                __syncwarp();
+                // rows 4*lane .. 4*lane+3: atom (lane / 2), half (lane & 1) of it
+                const uint32_t row_off = (uint32_t)(lane >> 1) * 1024 + (uint32_t)(lane & 1) * 512;
+                for (int c = c0; c < c0 + nck; ++c) {
+                    uint8_t *dst = tile + c * kChunkBytes + row_off;
+                    if (any) {
+                        tma_gather4(dst, kvmap, &full[g], c * 64, y[0], y[1], y[2], y[3]);
                     } else {
-                        col = c * 64 + gr * 8;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            *(uint4 *)(dst + e * 16) = make_uint4(0, 0, 0, 0);
                     }
-                    if (a < 0) bytes = 0;
-                    const uint16_t *src = bytes ? kv + a + col : kv;
-                    cp_async_16(tile + c * kChunkBytes + swz128(kr, gr), src, bytes);
                 }
-                cp_async_arrive(&full[g]);
+                if (!any) fence_proxy_async();
+                mbar_arrive(&full[g]);
             }
-            __syncwarp();
         }
-        // drain: every issued copy lands before shared memory is released
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =================
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, kHeads, false, false);
             const uint32_t idO = idesc_bf16(128, kHeads, true, true);
             const uint32_t tile_a = smem_u32(tile), q_a = smem_u32(qs), p_a = smem_u32(pslot);
-            for (int li = 0; li < ntiles; ++li) {
-                bool ok = true;
+            bool ok = ntiles == 0 || mbar_wait(q_full, 0, KID_MLA, abort_flag);
+            for (int li = 0; li < ntiles && ok; ++li) {
                 // S^T = C . Q^T over all chunks, group by group as the gathers land
                 bool first = true;
                 for (int g = 0; g < ngroups && ok; ++g) {
                     ok = mbar_wait(&full[g], li & 1, KID_MLA, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    fence_proxy_async();
                     const bool is_rope = (g == ngroups - 1);
                     const int c0 = is_rope ? rope : 2 * g;
                     const int nck = is_rope ? 1 : min(2, nv - 2 * g);
@@ -329,12 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
         for (int li = 0; li < ntiles; ++li) {
             // every decision that guards a named barrier or a warp-collective TMEM access
             // is made uniform over the 128 threads first
-            const bool got = mbar_wait(s_full, li & 1, KID_MLA, abort_flag);
+            const bool got = mbar_wait(&addr_ready[li & 1], (li >> 1) & 1, KID_MLA, abort_flag) &&
+                             mbar_wait(s_full, li & 1, KID_MLA, abort_flag);
             if (named_bar_or(2, kSoftmaxThreads, !got)) { ok = false; break; }
             tc_fence_after();
-            const int j = (t_begin + li) * kTileKeys + kl;
-            bool valid = false;
-            if (j < p.k) valid = resolve_row(p.layout, b, idx_row[j]) >= 0;
+            const bool valid = rows_sm[(li & 1) * kTileKeys + kl] >= 0;
             float x[64];
             tmem_ld64(tS + lane_addr, x);
 #pragma unroll
@@ -379,8 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
             if (any && li > 0) {
                 // rescale the running O (needs the previous tile's O product complete)
                 const bool got_o = mbar_wait(o_done, (li - 1) & 1, KID_MLA, abort_flag);
-                if (named_bar_or(2, kSoftmaxThreads, !got_o)) { ok = false; }
-                else {
+                if (named_bar_or(2, kSoftmaxThreads, !got_o)) {
+                    ok = false;
+                } else {
                     tc_fence_after();
                     for (int mb = 0; mb < nmb; ++mb) {
                         uint32_t v[32];
@@ -416,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
         if (kl < kHeads) lsum[kl] = red[kl] + red[64 + kl] + red[128 + kl] + red[192 + kl];
         named_bar_sync(1, kSoftmaxThreads);
         const int unit_out = row * p.layers + layer;
+        const bool have_o = ok && ntiles > 0;
         if (p.splits == 1) {
             uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
             for (int mb = 0; mb < nmb; ++mb) {
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
-                    if (ok && ntiles > 0) {
+                    if (have_o) {
                         tmem_ld32(tO + lane_addr + mb * kHeads + half * 32, v);
                         tmem_ld_wait();
                     } else {
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
-                    if (ok && ntiles > 0) {
+                    if (have_o) {
                         tmem_ld32(tO + lane_addr + mb * kHeads + half * 32, v);
                         tmem_ld_wait();
                     } else {
@@ -483,43 +488,50 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaParams
     if (warp == kMmaWarp) tmem_dealloc(tmem, tmem_cols);
 }
 
-// Merge split-KV partials: per head, weights 2^(R_s - R_max) on the partial sums.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p) {
-    const int unit = blockIdx.x;  // row * layers + layer
+// Merge split-KV partials of one (row, layer, head): weights 2^(R_s - R_max) on the
+// partial sums.  One CTA per (unit, head); each thread owns 4 consecutive dims.
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const MlaParams p) {
+    const int h = blockIdx.x % kHeads;
+    const int unit = blockIdx.x / kHeads;  // row * layers + layer
+    if (h >= p.H) return;
     const int layer = unit % p.layers;
     const int row = unit / p.layers;
     const size_t stride = (size_t)(kHeads * p.d + 2 * kHeads);
     const float *part = p.partial + (int64_t)unit * p.splits * stride;
-    __shared__ float wsc[32][kHeads];  // splits <= 32
-    __shared__ float rmax_s[kHeads], ltot_s[kHeads];
-    const int tid = threadIdx.x;
-    if (tid < kHeads) {
-        float rmax = -INFINITY;
-        for (int s = 0; s < p.splits; ++s) rmax = fmaxf(rmax, part[s * stride + kHeads * p.d + tid]);
-        float ltot = 0.f;
+    float rs[32], ws[32];
+    float rmax = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) {
+        rs[s] = __ldg(part + s * stride + kHeads * p.d + h);
+        rmax = fmaxf(rmax, rs[s]);
+    }
+    float ltot = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+        ws[s] = (rmax == -INFINITY || rs[s] == -INFINITY) ? 0.f : ex2_approx(rs[s] - rmax);
+        ltot = fmaf(ws[s], __ldg(part + s * stride + kHeads * p.d + kHeads + h), ltot);
+    }
+    const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+    uint16_t *out = p.out[layer] + ((int64_t)row * p.H + h) * p.d;
+    for (int d0 = threadIdx.x * 4; d0 < p.d; d0 += kCombineThreads * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < p.splits; ++s) {
-            const float r = part[s * stride + kHeads * p.d + tid];
-            const float w = (rmax == -INFINITY || r == -INFINITY) ? 0.f : ex2_approx(r - rmax);
-            wsc[s][tid] = w;
-            ltot += w * part[s * stride + kHeads * p.d + kHeads + tid];
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(part + s * stride + (int64_t)h * p.d + d0));
+            acc.x = fmaf(ws[s], v.x, acc.x);
+            acc.y = fmaf(ws[s], v.y, acc.y);
+            acc.z = fmaf(ws[s], v.z, acc.z);
+            acc.w = fmaf(ws[s], v.w, acc.w);
         }
-        rmax_s[tid] = rmax;
-        ltot_s[tid] = ltot;
+        const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        const __nv_bfloat162 c = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t *>(&a);
+        pk.y = *reinterpret_cast<const uint32_t *>(&c);
+        *reinterpret_cast<uint2 *>(out + d0) = pk;
     }
-    __syncthreads();
-    uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
-    for (int e = tid; e < p.H * p.d; e += blockDim.x) {
-        const int h = e / p.d, dim = e - h * p.d;
-        float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s) acc = fmaf(wsc[s][h], part[s * stride + (int64_t)h * p.d + dim], acc);
-        const float l = ltot_s[h];
-        out[e] = __bfloat16_as_ushort(__float2bfloat16_rn(l > 0.f ? acc / l : 0.f));
-    }
-    if (tid < p.H && p.lse[layer]) {
-        const float l = ltot_s[tid];
-        p.lse[layer][(int64_t)row * p.H + tid] =
-            l > 0.f ? (rmax_s[tid] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-    }
+    if (threadIdx.x == 0 && p.lse[layer])
+        p.lse[layer][(int64_t)row * p.H + h] =
+            ltot > 0.f ? (rmax + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace
@@ -540,7 +552,7 @@ size_t mla_partial_bytes(int units, int splits, int d) {
     return (size_t)units * splits * (size_t)(kHeads * d + 2 * kHeads) * sizeof(float);
 }
 
-cudaError_t launch_sparse_mla(const MlaParams &p, cudaStream_t stream) {
+cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream) {
     const int nch = p.d / 64 + 1;
     const MlaSmem L = mla_smem(nch);
     const size_t bytes = L.total + 1024;
@@ -554,10 +566,10 @@ cudaError_t launch_sparse_mla(const MlaParams &p, cudaStream_t stream) {
     }
     const int units = p.B * p.T * p.layers;
     if (units <= 0) return cudaSuccess;
-    sparse_mla_kernel<<<units * p.splits, kThreads, bytes, stream>>>(p);
+    sparse_mla_kernel<<<units * p.splits, kThreads, bytes, stream>>>(maps, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;
-    mla_combine_kernel<<<units, 256, 0, stream>>>(p);
+    mla_combine_kernel<<<units * kHeads, kCombineThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
