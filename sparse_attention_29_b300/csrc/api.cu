@@ -206,15 +206,16 @@ dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const f
     if (ng > 16384) return DSA_ERR_UNSUPPORTED;
     p.num_groups = (int)ng;
     p.acc_cols = pow2_at_least(p.N);
-    p.num_acc = 512 / p.acc_cols;
-    if (p.num_acc > 4) p.num_acc = 4;
+    p.num_acc = 512 / p.acc_cols;  // every TMEM column: the MMA never waits on the epilogue
+    if (p.num_acc > 8) p.num_acc = 8;
 
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_tiled();
     if (!encode) return DSA_ERR_CUDA;
-    CUtensorMap kmap;
+    CUtensorMap kmap, kmap128;
     const cuuint64_t dims[2] = {(cuuint64_t)Di, (cuuint64_t)layout->num_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)Di};
     const cuuint32_t box[2] = {(cuuint32_t)Di, 64};
+    const cuuint32_t box128[2] = {(cuuint32_t)Di, 128};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = Di == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : Di == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -222,10 +223,27 @@ dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const f
     CUresult cr = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(k8_cache),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return DSA_ERR_CUDA;
+    CUresult cr2 = encode(&kmap128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                          const_cast<uint8_t *>(k8_cache), dims, strides, box128, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS || cr2 != CUDA_SUCCESS) return DSA_ERR_CUDA;
+    // query codes: one box of N rows = G query rows x Hi heads (needs Hi == HP)
+    CUtensorMap qmap;
+    std::memset(&qmap, 0, sizeof qmap);
+    p.q_tma = (Hi == HP) ? 1 : 0;
+    if (p.q_tma) {
+        if ((int64_t)B * T * Hi >= ((int64_t)1 << 31) - 256) return DSA_ERR_UNSUPPORTED;
+        const cuuint64_t qdims[2] = {(cuuint64_t)Di, (cuuint64_t)B * T * Hi};
+        const cuuint32_t qbox[2] = {(cuuint32_t)Di, (cuuint32_t)p.N};
+        CUresult cr3 = encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(q8),
+                              qdims, strides, qbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr3 != CUDA_SUCCESS) return DSA_ERR_CUDA;
+    }
     const int sms = current_sm_count();
     if (sms <= 0) return DSA_ERR_CUDA;
-    return from_cuda(launch_indexer(p, kmap, sms, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_indexer(p, kmap, kmap128, qmap, sms, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int Lmax, int k,

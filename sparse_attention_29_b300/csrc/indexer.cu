@@ -14,34 +14,52 @@
 // The key cache streams through a TMA ring of 128-row tiles (HBM-bound for decode);
 // the query group sits in shared memory (double-buffered across groups).
 //
-// Roles (192 threads): warp 0 loads (TMA for keys, plain loads for the query group),
-// warp 1 issues the MMAs, warps 2-5 run the epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31).  CTAs are persistent: the tiles of all query groups form one list
-// and each CTA takes a contiguous slice of it, so ragged contexts balance evenly.
+// Roles (320 threads): warp 0 produces (it resolves the cache rows of 32 tiles at a time,
+// one lane per tile, then issues the TMA key loads, the query-group loads and cp.async
+// copies of the key scales into a small ring), warp 1 issues the MMAs, warps 2-9 run the
+// epilogue in two sets of four that take alternate tiles (warp w reads TMEM lanes
+// 32*(w%4) .. +31), so that every SM sub-partition has two epilogue warps to switch
+// between.  Nothing on the per-tile path waits on a global load.  CTAs are persistent: the tiles of all query groups form one list and
+// each CTA takes a contiguous slice of it, so ragged contexts balance evenly.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiSets = 2;                     // epilogue warp sets (alternate tiles)
+constexpr int kEpiWarps = 4 * kEpiSets;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue warps
 constexpr int kTileKeys = 128;
 constexpr int kBoxRows = 64;
 
 struct Smem {
     // offsets (bytes) from the 1024-aligned dynamic shared memory base
-    uint32_t kstage, qbuf, qbuf_bytes, wbuf, gpos, prefix, bars, total;
+    uint32_t kstage, qbuf, qbuf_bytes, ksring, wbuf, gpos, prefix, bars, total;
+    int ring;
 };
 
-__host__ __device__ inline Smem smem_layout(int Di, int N, int G, int stages, int num_groups,
+constexpr int kBatch = 32;  // tiles the producer resolves at once (one lane per tile)
+
+// Key-scale ring slots.  The producer fills a tile's slot when it issues the tile's key
+// load, after the stage-free wait for tile (it - stages); by then the epilogue has
+// finished every tile up to (it - stages - num_acc), so this many slots are never overrun.
+__host__ __device__ inline int ks_ring_slots(int stages, int num_acc) {
+    return stages + num_acc + 1;
+}
+
+__host__ __device__ inline Smem smem_layout(int Di, int N, int stages, int num_groups,
                                             int num_acc) {
     Smem s;
+    s.ring = ks_ring_slots(stages, num_acc);
     uint32_t off = 0;
     s.kstage = off;
     off += (uint32_t)stages * kTileKeys * Di;
     s.qbuf = off;
     s.qbuf_bytes = ((uint32_t)N * Di + 1023u) & ~1023u;
     off += 2 * s.qbuf_bytes;
+    s.ksring = off;
+    off += (uint32_t)s.ring * kTileKeys * 4;
     s.wbuf = off;
     off += 2 * (uint32_t)N * 4;
     s.gpos = off;
@@ -49,9 +67,8 @@ __host__ __device__ inline Smem smem_layout(int Di, int N, int G, int stages, in
     s.prefix = off;
     off += ((uint32_t)num_groups + 1 + 3) / 4 * 16;
     s.bars = off;
-    off += (uint32_t)(2 * stages + 4 + 2 * num_acc + 1) * 8 + 16;  // + abort flag, tmem base
+    off += (uint32_t)(2 * stages + 4 + 2 * num_acc + 1 + s.ring) * 8 + 16;  // + flag, tmem
     s.total = off;
-    (void)G;
     return s;
 }
 
@@ -68,21 +85,25 @@ struct TileCursor {
     const int *prefix;
     int num_groups;
     int g, j, t, te;
-    __device__ void init(const int *pre, int ng, int tb, int te_) {
+    __device__ void init(const int *pre, int ng, int t0, int te_) {
         prefix = pre;
         num_groups = ng;
-        t = tb;
+        t = t0;
         te = te_;
-        // the group holding tile tb: last g with prefix[g] <= tb (skipping empty groups)
+        if (t0 >= te_) {
+            g = ng;
+            j = 0;
+            return;
+        }
+        // the group holding tile t0: last g with prefix[g] <= t0 (skipping empty groups)
         int lo = 0, hi = ng - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (pre[mid] <= tb) lo = mid;
+            if (pre[mid] <= t0) lo = mid;
             else hi = mid - 1;
         }
         g = lo;
-        while (g < ng - 1 && pre[g + 1] <= tb) ++g;
-        j = tb - pre[g];
+        j = t0 - pre[g];
     }
     __device__ bool valid() const { return t < te; }
     __device__ int tiles_in_group() const { return prefix[g + 1] - prefix[g]; }
@@ -98,18 +119,75 @@ struct TileCursor {
     }
 };
 
-template <int DI>
+// Walks the groups of a CTA's tile range [tb, tb + n) in order: `g` is the group of the
+// current tile; at_start/is_last say whether tile `it` (relative) starts or ends its group
+// within the range.  One compare per tile; empty groups are skipped at boundaries.
+struct GroupWalk {
+    const int *prefix;
+    int num_groups, tb, n, g, next_start;  // next_start: relative index of the next group
+    __device__ void init(const int *pre, int ng, int tb_, int n_) {
+        prefix = pre;
+        num_groups = ng;
+        tb = tb_;
+        n = n_;
+        int lo = 0, hi = ng - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= tb_) lo = mid;
+            else hi = mid - 1;
+        }
+        g = lo;
+        next_start = pre[g + 1] - tb_;
+    }
+    __device__ bool at_start(int it) const { return it == 0 || it == prev_end_; }
+    __device__ bool is_last(int it) const { return it + 1 == next_start || it + 1 == n; }
+    __device__ void step(int it) {
+        if (it + 1 == next_start && it + 1 < n) {
+            prev_end_ = it + 1;
+            do {
+                ++g;
+                next_start = prefix[g + 1] - tb;
+            } while (next_start == it + 1 && g + 1 < num_groups);
+        }
+    }
+    int prev_end_ = -1;
+};
+
+// Largest valid position among the rows of query group g (-1 if none).
+__device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool report) {
+    const int b = g / p.groups_per_seq;
+    const int gi = g - b * p.groups_per_seq;
+    const int r0 = b * p.T + gi * p.G;
+    const int nr = min(p.G, p.T - gi * p.G);
+    int maxpos = -1;
+    for (int i = 0; i < nr; ++i) {
+        const int pos = __ldg(p.q_pos + r0 + i);
+        if (pos < 0 || pos >= p.Lmax) {
+            if (report) record_error(KID_INDEXER, ERR_BAD_POSITION);
+            continue;
+        }
+        maxpos = max(maxpos, pos);
+    }
+    return maxpos;
+}
+
+// kW64: decode form (one query row of 64 padded heads per group); its weights stay in
+// registers.  Otherwise they are read from shared memory.
+template <int DI, bool kW64>
 __global__ void __launch_bounds__(kThreads, 1)
-    indexer_kernel(const __grid_constant__ CUtensorMap kmap, const IndexerParams p) {
+    indexer_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap kmap128,
+                   const __grid_constant__ CUtensorMap qmap, const IndexerParams p) {
     constexpr int kTileBytes = kTileKeys * DI;
     constexpr uint32_t kLayout = DI == 128 ? kLayoutSW128 : (DI == 64 ? kLayoutSW64 : kLayoutSW32);
     constexpr uint32_t kSBO = 8 * DI;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Smem L = smem_layout(DI, p.N, p.G, p.stages, p.num_groups, p.num_acc);
+    const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc);
     uint8_t *kstage = smem + L.kstage;
     uint8_t *qbuf = smem + L.qbuf;
+    float *ksring = (float *)(smem + L.ksring);
     float *wbuf = (float *)(smem + L.wbuf);
     int *gpos = (int *)(smem + L.gpos);
     int *prefix = (int *)(smem + L.prefix);
@@ -121,8 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *accfull = qempty + 2;
     uint64_t *accempty = accfull + p.num_acc;
     uint64_t *drain = accempty + p.num_acc;
-    volatile int *abort_flag = (volatile int *)(drain + 1);
-    uint32_t *tmem_base_sm = (uint32_t *)(drain + 1) + 1;
+    uint64_t *ksfull = drain + 1;
+    volatile int *abort_flag = (volatile int *)(ksfull + L.ring);
+    uint32_t *tmem_base_sm = (uint32_t *)(ksfull + L.ring) + 1;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -130,44 +209,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- tile list: tiles of each query group, prefix-summed -------------------------
     {
-        __shared__ int partial[kThreads];
+        int *warp_sum = reinterpret_cast<int *>(kstage);  // scratch: the key ring is unused yet
         const int ng = p.num_groups;
         const int per = (ng + kThreads - 1) / kThreads;
         const int lo = min(tid * per, ng), hi = min(lo + per, ng);
-        auto group_tiles = [&](int g) -> int {
-            const int b = g / p.groups_per_seq;
-            const int gi = g - b * p.groups_per_seq;
-            const int r0 = b * p.T + gi * p.G;
-            const int nr = min(p.G, p.T - gi * p.G);
-            int maxpos = -1;
-            for (int i = 0; i < nr; ++i) {
-                const int pos = p.q_pos[r0 + i];
-                if (pos < 0 || pos >= p.Lmax) {
-                    if (blockIdx.x == 0) record_error(KID_INDEXER, ERR_BAD_POSITION);
-                    continue;
-                }
-                maxpos = max(maxpos, pos);
-            }
-            return (maxpos + kTileKeys) / kTileKeys;
-        };
         int local = 0;
-        for (int g = lo; g < hi; ++g) local += group_tiles(g);
-        partial[tid] = local;
+        for (int g = lo; g < hi; ++g) {
+            const int n = (group_maxpos(p, g, blockIdx.x == 0) + kTileKeys) / kTileKeys;
+            prefix[g] = n;  // counts first, offsets below
+            local += n;
+        }
+        // block-wide exclusive scan of the per-thread sums
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
         __syncthreads();
-        if (tid == 0) {
-            int run = 0;
-            for (int i = 0; i < kThreads; ++i) {
-                const int v = partial[i];
-                partial[i] = run;
-                run += v;
+        if (warp == 0) {
+            const int v = lane < kThreads / 32 ? warp_sum[lane] : 0;
+            int x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
             }
-            prefix[ng] = run;
+            if (lane < kThreads / 32) warp_sum[lane] = x - v;
+            if (lane == kThreads / 32 - 1) prefix[ng] = x;
         }
         __syncthreads();
-        int run = partial[tid];
+        int run = warp_sum[warp] + incl - local;
         for (int g = lo; g < hi; ++g) {
+            const int n = prefix[g];
             prefix[g] = run;
-            run += group_tiles(g);
+            run += n;
         }
         __syncthreads();
     }
@@ -175,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tb = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
     const int te = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
     if (tb >= te) return;
+    const int ntile = te - tb;
 
     // ---- barriers, tensor memory -----------------------------------------------------
     if (tid == 0) {
@@ -183,13 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&qfull[i], 1);
-            mbar_init(&qempty[i], 1 + 4);
+            mbar_init(&qfull[i], 32);  // every producer lane (lane 0 also adds the TMA bytes)
+            mbar_init(&qempty[i], 1 + kEpiWarps);  // MMA + every epilogue warp
         }
         for (int i = 0; i < p.num_acc; ++i) {
             mbar_init(&accfull[i], 1);
             mbar_init(&accempty[i], 4);
         }
+        for (int i = 0; i < L.ring; ++i) mbar_init(&ksfull[i], 32);  // every producer lane
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -198,7 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_base_sm, (uint32_t)(p.acc_cols * p.num_acc));
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) prefetch_tmap(&kmap);
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&kmap128);
+        if (p.q_tma) prefetch_tmap(&qmap);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -206,104 +289,166 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================= producer =================
-        TileCursor cur;
-        cur.init(prefix, p.num_groups, tb, te);
-        int it = 0, gcount = 0, issued = 0;
-        bool ok = true;
-        for (; cur.valid() && ok; cur.next(), ++it) {
-            const int b = cur.g / p.groups_per_seq;
-            if (cur.first_in_range(tb)) {
-                const int slot = gcount & 1, use = gcount >> 1;
-                if (use > 0) ok = mbar_wait(&qempty[slot], (use - 1) & 1, KID_INDEXER, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                // query group -> qbuf[slot]: row n = qi*HP + h, zero rows for padding
-                const int gi = cur.g - b * p.groups_per_seq;
-                const int r0 = b * p.T + gi * p.G;
-                const int nr = min(p.G, p.T - gi * p.G);
-                uint8_t *qdst = qbuf + slot * L.qbuf_bytes;
-                const int grans = DI / 16;
+        // query group g -> slot: q codes by TMA (rows n = qi*HP + h) when the heads need no
+        // padding, else plain loads with zero rows; weights * q_scale and positions by the
+        // lanes.  Every lane arrives on qfull[slot]; lane 0 also adds the TMA bytes.
+        auto load_group = [&](int g, int slot) {
+            const int b = g / p.groups_per_seq;
+            const int gi = g - b * p.groups_per_seq;
+            const int r0 = b * p.T + gi * p.G;
+            const int nr = min(p.G, p.T - gi * p.G);
+            uint8_t *qdst = qbuf + slot * L.qbuf_bytes;
+            if (p.q_tma) {
+                if (lane == 0) {
+                    mbar_expect_tx(&qfull[slot], (uint32_t)(p.N * DI));
+                    tma_load_2d(qdst, &qmap, &qfull[slot], 0, r0 * p.Hi);
+                }
+            } else {
+                constexpr int grans = DI / 16;
                 for (int e = lane; e < p.N * grans; e += 32) {
                     const int n = e / grans, gr = e - n * grans;
                     const int qi = n / p.HP, h = n - qi * p.HP;
                     uint4 v = make_uint4(0, 0, 0, 0);
                     if (qi < nr && h < p.Hi)
-                        v = *(const uint4 *)(p.q8 + (((int64_t)(r0 + qi) * p.Hi + h) * DI) + gr * 16);
-                    const int atom = n >> 3;
-                    *(uint4 *)(qdst + atom * kSBO + swz_off(n & 7, gr, DI)) = v;
-                }
-                float *wdst = wbuf + slot * p.N;
-                for (int n = lane; n < p.N; n += 32) {
-                    const int qi = n / p.HP, h = n - qi * p.HP;
-                    float v = 0.f;
-                    if (qi < nr && h < p.Hi)
-                        v = p.w[(int64_t)(r0 + qi) * p.Hi + h] * p.q_scale[r0 + qi];
-                    wdst[n] = v;
-                }
-                if (lane < 16) {
-                    int pos = -1;
-                    if (lane < nr) {
-                        pos = p.q_pos[r0 + lane];
-                        if (pos < 0 || pos >= p.Lmax) pos = -1;
-                    }
-                    gpos[slot * 16 + lane] = pos;
+                        v = __ldg((const uint4 *)(p.q8 + (((int64_t)(r0 + qi) * p.Hi + h) * DI) + gr * 16));
+                    *(uint4 *)(qdst + (n >> 3) * kSBO + swz_off(n & 7, gr, DI)) = v;
                 }
                 fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&qfull[slot]);
-                ++gcount;
             }
-            if (lane == 0) {
-                const int stage = it % p.stages, use = it / p.stages;
-                if (use > 0) ok = mbar_wait(&kempty[stage], (use - 1) & 1, KID_INDEXER, abort_flag);
-                if (ok) {
-                    const int s0 = cur.j * kTileKeys;
-                    const int maxpos = [&] {
-                        int m = -1;
-                        const int gi = cur.g - b * p.groups_per_seq;
-                        const int r0 = b * p.T + gi * p.G;
-                        const int nr = min(p.G, p.T - gi * p.G);
-                        for (int i = 0; i < nr; ++i) m = max(m, p.q_pos[r0 + i]);
-                        return m;
-                    }();
-                    int ys[2];
-                    int nbox = 0;
+            float *wdst = wbuf + slot * p.N;
+            for (int n = lane; n < p.N; n += 32) {
+                const int qi = n / p.HP, h = n - qi * p.HP;
+                float v = 0.f;
+                if (qi < nr && h < p.Hi)
+                    v = __ldg(p.w + (int64_t)(r0 + qi) * p.Hi + h) * __ldg(p.q_scale + r0 + qi);
+                wdst[n] = v;
+            }
+            if (lane < 16) {
+                int pos = -1;
+                if (lane < nr) {
+                    pos = __ldg(p.q_pos + r0 + lane);
+                    if (pos < 0 || pos >= p.Lmax) pos = -1;
+                }
+                gpos[slot * 16 + lane] = pos;
+            }
+            __syncwarp();
+            mbar_arrive(&qfull[slot]);
+        };
+        // the range's first group goes out before anything else
+        {
+            TileCursor c0;
+            c0.init(prefix, p.num_groups, tb, te);
+            load_group(c0.g, 0);
+        }
+        int it = 0, gcount = 1, issued = 0;
+        int pstage = 0, pslot = 0;
+        uint32_t pphase = 0;
+        bool ok = true;
+        while (ok && it < ntile) {
+            const int nb = min(kBatch, ntile - it);
+            // ---- lane l resolves tile it + l: box rows, group start, scale rows ----
+            int l_g = 0, l_newg = 0, l_nbox = 0, l_y0 = 0, l_y1 = 0, l_r0 = -1, l_r1 = -1;
+            if (lane < nb) {
+                TileCursor c;
+                c.init(prefix, p.num_groups, tb + it + lane, te);
+                l_g = c.g;
+                l_newg = c.first_in_range(tb) && (it + lane > 0);  // the first is loaded
+                const int b = c.g / p.groups_per_seq;
+                const int s0 = c.j * kTileKeys;
+                // issue every address load before using any of them
+                int64_t yb[2];
+                if (p.layout.block_table) {
                     for (int hb = 0; hb < 2; ++hb) {
-                        const int s = s0 + hb * kBoxRows;
-                        if (s > maxpos) break;
-                        int64_t y;
-                        if (p.layout.block_table) {
-                            const int lp = s / p.layout.page_size;
-                            const int page = lp < p.layout.pages_per_seq
-                                ? p.layout.block_table[(int64_t)b * p.layout.pages_per_seq + lp] : -1;
-                            if (page < 0 || (int64_t)page * p.layout.page_size >= p.layout.num_rows) {
-                                record_error(KID_INDEXER, ERR_BAD_PAGE);
-                                y = -2 * kBoxRows;  // wholly outside: TMA fills zeros
-                            } else {
-                                y = (int64_t)page * p.layout.page_size + s % p.layout.page_size;
-                            }
-                        } else {
-                            y = (int64_t)p.layout.seq_start[b] + s;
-                            if (y < 0 || y >= p.layout.num_rows) {
-                                record_error(KID_INDEXER, ERR_BAD_INDEX);
-                                y = -2 * kBoxRows;
-                            }
-                        }
-                        ys[nbox++] = (int)y;
+                        const int lp = (s0 + hb * kBoxRows) / p.layout.page_size;
+                        const int page = lp < p.layout.pages_per_seq
+                            ? __ldg(p.layout.block_table + (int64_t)b * p.layout.pages_per_seq + lp) : -1;
+                        yb[hb] = page < 0 ? -1
+                                          : (int64_t)page * p.layout.page_size + (s0 + hb * kBoxRows) % p.layout.page_size;
                     }
-                    uint8_t *dst = kstage + stage * kTileBytes;
-                    mbar_arrive_expect_tx(&kfull[stage], (uint32_t)(nbox * kBoxRows * DI));
-                    for (int hb = 0; hb < nbox; ++hb)
-                        tma_load_2d(dst + hb * kBoxRows * DI, &kmap, &kfull[stage], 0, ys[hb]);
-                    issued = it + 1;
+                } else {
+                    const int64_t st = __ldg(p.layout.seq_start + b);
+                    yb[0] = st + s0;
+                    yb[1] = st + s0 + kBoxRows;
+                }
+                const int maxpos = group_maxpos(p, c.g, false);
+                int ys[2], rs[2];
+                for (int hb = 0; hb < 2; ++hb) {
+                    ys[hb] = 0;
+                    rs[hb] = -1;
+                    if (s0 + hb * kBoxRows > maxpos) continue;
+                    const int64_t y = yb[hb];
+                    const bool good = y >= 0 && y < p.layout.num_rows;
+                    if (!good) record_error(KID_INDEXER, p.layout.block_table ? ERR_BAD_PAGE : ERR_BAD_INDEX);
+                    ys[hb] = good ? (int)y : -2 * kBoxRows;  // wholly outside: TMA fills zeros
+                    rs[hb] = good ? (int)y : -1;
+                    ++l_nbox;
+                }
+                l_y0 = ys[0];
+                l_y1 = ys[1];
+                l_r0 = rs[0];
+                l_r1 = rs[1];
+            }
+            // ---- issue the batch in order ----
+            for (int t = 0; t < nb; ++t, ++it) {
+                const int g = __shfl_sync(0xffffffffu, l_g, t);
+                if (__shfl_sync(0xffffffffu, l_newg, t)) {
+                    const int slot = gcount & 1, use = gcount >> 1;
+                    if (use > 0) ok = mbar_wait(&qempty[slot], (use - 1) & 1, KID_INDEXER, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    load_group(g, slot);
+                    ++gcount;
+                }
+                const int nbox = __shfl_sync(0xffffffffu, l_nbox, t);
+                const int y0 = __shfl_sync(0xffffffffu, l_y0, t);
+                const int y1 = __shfl_sync(0xffffffffu, l_y1, t);
+                const int r0k = __shfl_sync(0xffffffffu, l_r0, t);
+                const int r1k = __shfl_sync(0xffffffffu, l_r1, t);
+                if (lane == 0) {
+                    const int stage = pstage;
+                    if (it >= p.stages) ok = mbar_wait(&kempty[stage], pphase ^ 1u, KID_INDEXER, abort_flag);
+                    if (ok) {
+                        uint8_t *dst = kstage + stage * kTileBytes;
+                        mbar_arrive_expect_tx(&kfull[stage], (uint32_t)(nbox * kBoxRows * DI));
+                        if (nbox == 2 && y1 == y0 + kBoxRows) {
+                            tma_load_2d(dst, &kmap128, &kfull[stage], 0, y0);  // one 128-row box
+                        } else {
+                            if (nbox > 0) tma_load_2d(dst, &kmap, &kfull[stage], 0, y0);
+                            if (nbox > 1) tma_load_2d(dst + kBoxRows * DI, &kmap, &kfull[stage], 0, y1);
+                        }
+                        issued = it + 1;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (++pstage == p.stages) { pstage = 0; pphase ^= 1u; }
+                // this tile's key scales -> ring slot (free: see ks_ring_slots); 4 per lane
+                {
+                    const int slot = pslot;
+                    if (++pslot == L.ring) pslot = 0;
+                    float *ks = ksring + slot * kTileKeys + lane * 4;
+                    const int k = lane * 4;
+                    const int base = k < kBoxRows ? r0k : r1k;
+                    const int64_t row = base < 0 ? -1 : (int64_t)base + (k & (kBoxRows - 1));
+                    if (row >= 0 && row + 4 <= p.layout.num_rows &&
+                        (reinterpret_cast<uintptr_t>(p.k_scale + row) & 15) == 0) {
+                        cp_async_16(ks, p.k_scale + row, 16u);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bool good = row >= 0 && row + e < p.layout.num_rows;
+                            cp_async_4(ks + e, good ? p.k_scale + row + e : p.k_scale, good ? 4u : 0u);
+                        }
+                    }
+                    cp_async_arrive(&ksfull[slot]);
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        // drain: every issued key load must land before the CTA's shared memory goes away
+        // drain: every issued copy must land before the CTA's shared memory goes away
+        asm volatile("cp.async.wait_all;" ::: "memory");
         if (lane == 0) {
             for (int st = 0; st < p.stages && st < issued; ++st) {
-                const int last_use = (issued - 1 - st) / p.stages;  // uses of stage st: 0..last_use
+                const int last_use = (issued - 1 - st) / p.stages;
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(&kfull[st], last_use & 1) &&
                        globaltimer_ns() - t0 < kWaitLimitNs) {
@@ -312,36 +457,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
+        // Per tile: stage, accumulator and phases advance by counters; the group changes
+        // when the tile index reaches the next group's first tile (one compare per tile).
         if (lane == 0) {
-            TileCursor cur;
-            cur.init(prefix, p.num_groups, tb, te);
             const uint32_t idesc = idesc_e4m3(128, p.N);
-            int it = 0, gcount = 0, slot = 0;
-            for (; cur.valid(); cur.next(), ++it) {
-                if (cur.first_in_range(tb)) {
-                    slot = gcount & 1;
-                    if (!mbar_wait(&qfull[slot], (gcount >> 1) & 1, KID_INDEXER, abort_flag)) break;
+            const uint64_t adesc0 = make_sdesc(smem_u32(kstage), 16, kSBO, kLayout);
+            const uint64_t bdesc0 = make_sdesc(smem_u32(qbuf), 16, kSBO, kLayout);
+            GroupWalk gw;
+            gw.init(prefix, p.num_groups, tb, ntile);
+            int stage = 0, abuf = 0, gcount = 0, qslot = 0;
+            uint32_t kphase = 0, aphase = 0;
+            bool ok = true;
+            for (int it = 0; it < ntile && ok; ++it) {
+                if (gw.at_start(it)) {
+                    qslot = gcount & 1;
+                    ok = mbar_wait(&qfull[qslot], (gcount >> 1) & 1, KID_INDEXER, abort_flag);
                     ++gcount;
+                    if (!ok) break;
                 }
-                const int stage = it % p.stages;
-                if (!mbar_wait(&kfull[stage], (it / p.stages) & 1, KID_INDEXER, abort_flag)) break;
-                const int abuf = it % p.num_acc, ause = it / p.num_acc;
-                if (ause > 0 &&
-                    !mbar_wait(&accempty[abuf], (ause - 1) & 1, KID_INDEXER, abort_flag))
-                    break;
+                ok = mbar_wait(&kfull[stage], kphase, KID_INDEXER, abort_flag);
+                if (ok && it >= p.num_acc)
+                    ok = mbar_wait(&accempty[abuf], aphase ^ 1u, KID_INDEXER, abort_flag);
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(kstage + stage * kTileBytes);
-                const uint32_t b0 = smem_u32(qbuf + slot * L.qbuf_bytes);
+                const uint32_t a_off = (uint32_t)(stage * kTileBytes) >> 4;
+                const uint32_t b_off = (uint32_t)(qslot * L.qbuf_bytes) >> 4;
                 const uint32_t d = tmem + (uint32_t)(abuf * p.acc_cols);
 #pragma unroll
-                for (int ks = 0; ks < DI / 32; ++ks) {
-                    const uint64_t ad = make_sdesc(a0 + ks * 32, 16, kSBO, kLayout);
-                    const uint64_t bd = make_sdesc(b0 + ks * 32, 16, kSBO, kLayout);
-                    mma_e4m3(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
-                }
+                for (int ks = 0; ks < DI / 32; ++ks)
+                    mma_e4m3(d, adesc0 + a_off + 2 * ks, bdesc0 + b_off + 2 * ks, idesc, ks > 0 ? 1u : 0u);
                 mma_commit(&kempty[stage]);
                 mma_commit(&accfull[abuf]);
-                if (cur.last_in_range()) mma_commit(&qempty[slot]);
+                if (gw.is_last(it)) mma_commit(&qempty[qslot]);
+                gw.step(it);
+                if (++stage == p.stages) { stage = 0; kphase ^= 1u; }
+                if (++abuf == p.num_acc) { abuf = 0; aphase ^= 1u; }
             }
             mma_commit(drain);
             const uint64_t t0 = globaltimer_ns();
@@ -352,135 +502,153 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================= epilogue =================
         const int quarter = warp & 3;
+        const int eset = (warp - 2) / 4;  // this warp takes tiles it with it % kEpiSets == eset
         const int key_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        // this thread's key scale for the tile at cursor c (0 if the row is invalid); the
-        // loads run two tiles ahead of their use, off the critical path
-        auto key_scale = [&](const TileCursor &c) -> float {
-            if (!c.valid()) return 0.f;
-            const int bb = c.g / p.groups_per_seq;
-            const int s = c.j * kTileKeys + key_in_tile;
-            int64_t row;
-            if (p.layout.block_table) {
-                const int lp = s / p.layout.page_size;
-                if (lp >= p.layout.pages_per_seq) return 0.f;
-                const int page = p.layout.block_table[(int64_t)bb * p.layout.pages_per_seq + lp];
-                if (page < 0) return 0.f;
-                row = (int64_t)page * p.layout.page_size + s % p.layout.page_size;
-            } else {
-                row = (int64_t)p.layout.seq_start[bb] + s;
-            }
-            return (row >= 0 && row < p.layout.num_rows) ? __ldg(p.k_scale + row) : 0.f;
-        };
-        TileCursor cur;
-        cur.init(prefix, p.num_groups, tb, te);
-        TileCursor ahead = cur;
-        float ksc_ring0 = key_scale(ahead);
-        ahead.next();
-        float ksc_ring1 = key_scale(ahead);
-        ahead.next();
-        int it = 0, gcount = 0, slot = 0;
-        for (; cur.valid(); cur.next(), ++it) {
-            const float ksc = ksc_ring0;
-            ksc_ring0 = ksc_ring1;
-            ksc_ring1 = key_scale(ahead);
-            ahead.next();
-            const int b = cur.g / p.groups_per_seq;
-            if (cur.first_in_range(tb)) {
+        float wr[kW64 ? 64 : 1];
+        GroupWalk gw;
+        gw.init(prefix, p.num_groups, tb, ntile);
+        int abuf = 0, kslot = 0, gcount = 0, slot = 0;
+        uint32_t aphase = 0, ksphase = 0;
+        int r0 = 0, nr = 0, gfirst = 0;  // current group: first row, rows, first tile (abs.)
+        for (int it = 0; it < ntile; ++it) {
+            if (gw.at_start(it)) {
                 slot = gcount & 1;
                 const bool got = mbar_wait(&qfull[slot], (gcount >> 1) & 1, KID_INDEXER, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: TMEM loads follow
                 ++gcount;
-            }
-            const int abuf = it % p.num_acc;
-            const bool got = mbar_wait(&accfull[abuf], (it / p.num_acc) & 1, KID_INDEXER, abort_flag);
-            if (!__all_sync(0xffffffffu, got)) break;
-            tc_fence_after();
-            const int gi = cur.g - b * p.groups_per_seq;
-            const int r0 = b * p.T + gi * p.G;
-            const int nr = min(p.G, p.T - gi * p.G);
-            const int s = cur.j * kTileKeys + key_in_tile;
-            const int *pos = gpos + slot * 16;
-            const float *wq = wbuf + slot * p.N;
-            const uint32_t tacc = tmem + lane_addr + (uint32_t)(abuf * p.acc_cols);
-            for (int qi = 0; qi < nr; ++qi) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
-                for (int c0 = 0; c0 < p.HP; c0 += 64) {
-                    uint32_t v[4][16];
-                    const int nchunk = min(4, (p.HP - c0) / 16);
+                const int g = gw.g;
+                const int b = g / p.groups_per_seq;
+                const int gi = g - b * p.groups_per_seq;
+                r0 = b * p.T + gi * p.G;
+                nr = min(p.G, p.T - gi * p.G);
+                gfirst = prefix[g];
+                if constexpr (kW64) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c < nchunk) tmem_ld16(tacc + (uint32_t)(qi * p.HP + c0 + c * 16), v[c]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < nchunk) {
-                            const float4 *w4 = (const float4 *)(wq + qi * p.HP + c0 + c * 16);
-#pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                const float4 ww = w4[e4];
-                                a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[c][e4 * 4 + 0]), 0.f), a0);
-                                a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[c][e4 * 4 + 1]), 0.f), a1);
-                                a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[c][e4 * 4 + 2]), 0.f), a2);
-                                a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[c][e4 * 4 + 3]), 0.f), a3);
-                            }
-                        }
+                    for (int h = 0; h < 64; h += 4) {
+                        const float4 v = *(const float4 *)(wbuf + slot * p.N + h);
+                        wr[h] = v.x;
+                        wr[h + 1] = v.y;
+                        wr[h + 2] = v.z;
+                        wr[h + 3] = v.w;
                     }
                 }
-                if (s <= pos[qi])
-                    p.scores[(int64_t)(r0 + qi) * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&accempty[abuf]);
-                if (cur.last_in_range()) mbar_arrive(&qempty[slot]);
+            if ((it & (kEpiSets - 1)) == eset) {
+                const bool got = mbar_wait(&accfull[abuf], aphase, KID_INDEXER, abort_flag) &&
+                                 mbar_wait(&ksfull[kslot], ksphase, KID_INDEXER, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) break;
+                tc_fence_after();
+                const float ksc = ksring[kslot * kTileKeys + key_in_tile];
+                const int s = (tb + it - gfirst) * kTileKeys + key_in_tile;
+                const int *pos = gpos + slot * 16;
+                const uint32_t tacc = tmem + lane_addr + (uint32_t)(abuf * p.acc_cols);
+                if constexpr (kW64) {
+                    uint32_t v[64];
+                    tmem_ld32(tacc, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
+                    tmem_ld32(tacc + 32, *reinterpret_cast<uint32_t (*)[32]>(&v[32]));
+                    tmem_ld_wait();
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 64; h += 4) {
+                        a0 = fmaf(wr[h + 0], fmaxf(__uint_as_float(v[h + 0]), 0.f), a0);
+                        a1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.f), a1);
+                        a2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(v[h + 2]), 0.f), a2);
+                        a3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(v[h + 3]), 0.f), a3);
+                    }
+                    if (s <= pos[0])
+                        p.scores[(int64_t)r0 * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
+                } else {
+                    const float *wq = wbuf + slot * p.N;
+                    for (int qi = 0; qi < nr; ++qi) {
+                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
+                        for (int c0 = 0; c0 < p.HP; c0 += 64) {
+                            uint32_t v[4][16];
+                            const int nchunk = min(4, (p.HP - c0) / 16);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if (c < nchunk) tmem_ld16(tacc + (uint32_t)(qi * p.HP + c0 + c * 16), v[c]);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                if (c < nchunk) {
+                                    const float4 *w4 = (const float4 *)(wq + qi * p.HP + c0 + c * 16);
+#pragma unroll
+                                    for (int e4 = 0; e4 < 4; ++e4) {
+                                        const float4 ww = w4[e4];
+                                        a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[c][e4 * 4 + 0]), 0.f), a0);
+                                        a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[c][e4 * 4 + 1]), 0.f), a1);
+                                        a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[c][e4 * 4 + 2]), 0.f), a2);
+                                        a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[c][e4 * 4 + 3]), 0.f), a3);
+                                    }
+                                }
+                            }
+                        }
+                        if (s <= pos[qi])
+                            p.scores[(int64_t)(r0 + qi) * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[abuf]);
             }
+            if (gw.is_last(it)) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qempty[slot]);
+            }
+            gw.step(it);
+            if (++abuf == p.num_acc) { abuf = 0; aphase ^= 1u; }
+            if (++kslot == L.ring) { kslot = 0; ksphase ^= 1u; }
         }
     }
-
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, (uint32_t)(p.acc_cols * p.num_acc));
 }
 
-template <int DI>
-cudaError_t launch_di(const IndexerParams &p, const CUtensorMap &kmap, int grid,
+template <int DI, bool kW64>
+cudaError_t launch_di(const IndexerParams &p, const CUtensorMap &kmap,
+                      const CUtensorMap &kmap128, const CUtensorMap &qmap, int grid,
                       cudaStream_t stream) {
-    const Smem L = smem_layout(DI, p.N, p.G, p.stages, p.num_groups, p.num_acc);
+    const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc);
     const size_t bytes = L.total + 1024;
     static int attr_set_bytes = 0;  // per process; max over calls
     if ((int)bytes > attr_set_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_kernel<DI>,
+        cudaError_t e = cudaFuncSetAttribute(indexer_kernel<DI, kW64>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)bytes);
         if (e != cudaSuccess) return e;
         attr_set_bytes = (int)bytes;
     }
-    indexer_kernel<DI><<<grid, kThreads, bytes, stream>>>(kmap, p);
+    indexer_kernel<DI, kW64><<<grid, kThreads, bytes, stream>>>(kmap, kmap128, qmap, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_indexer(const IndexerParams &p_in, const CUtensorMap &kmap, int num_sms,
+cudaError_t launch_indexer(const IndexerParams &p_in, const CUtensorMap &kmap,
+                           const CUtensorMap &kmap128, const CUtensorMap &qmap, int num_sms,
                            cudaStream_t stream) {
     IndexerParams p = p_in;
-    // shared-memory budget: key ring takes what the query buffers and tile list leave
+    // shared-memory budget: the key ring takes what the rest leaves, up to 12 stages
     const int budget = 227 * 1024 - 1024;
-    const Smem base = smem_layout(p.Di, p.N, p.G, 0, p.num_groups, p.num_acc);
-    const int per_stage = kTileKeys * p.Di + 16;
-    p.stages = (budget - (int)base.total) / per_stage;
-    if (p.stages > 12) p.stages = 12;
+    p.stages = 12;  // ~192 KB in flight per SM keeps HBM busy across the ~3-6 us load latency
+    while (p.stages >= 2 &&
+           (int)smem_layout(p.Di, p.N, p.stages, p.num_groups, p.num_acc).total > budget)
+        --p.stages;
     if (p.stages < 2) return cudaErrorInvalidConfiguration;
     const int64_t max_tiles = (int64_t)p.num_groups * ((p.Lmax + kTileKeys - 1) / kTileKeys);
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid <= 0) return cudaSuccess;
+    const bool w64 = (p.N == 64 && p.G == 1);
     switch (p.Di) {
-        case 32: return launch_di<32>(p, kmap, grid, stream);
-        case 64: return launch_di<64>(p, kmap, grid, stream);
-        case 128: return launch_di<128>(p, kmap, grid, stream);
+        case 32: return w64 ? launch_di<32, true>(p, kmap, kmap128, qmap, grid, stream)
+                            : launch_di<32, false>(p, kmap, kmap128, qmap, grid, stream);
+        case 64: return w64 ? launch_di<64, true>(p, kmap, kmap128, qmap, grid, stream)
+                            : launch_di<64, false>(p, kmap, kmap128, qmap, grid, stream);
+        case 128: return w64 ? launch_di<128, true>(p, kmap, kmap128, qmap, grid, stream)
+                             : launch_di<128, false>(p, kmap, kmap128, qmap, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

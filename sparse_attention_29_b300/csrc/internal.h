@@ -6,7 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/dsa.h"
+#include "dsa.h"
 
 namespace dsa {
 
@@ -43,9 +43,13 @@ struct IndexerParams {
     int acc_cols;  // TMEM columns per accumulator buffer
     int num_acc;   // accumulator buffers
     int stages;    // key pipeline depth
+    int q_tma;     // 1: query groups load by TMA (Hi == HP), 0: plain loads with padding
 };
 
-cudaError_t launch_indexer(const IndexerParams &p, const CUtensorMap &kmap, int num_sms,
+// kmap: 64-row key boxes (any layout); kmap128: 128-row boxes (contiguous runs);
+// qmap: query codes as [rows * Hi, Di] with N-row boxes (used when q_tma)
+cudaError_t launch_indexer(const IndexerParams &p, const CUtensorMap &kmap,
+                           const CUtensorMap &kmap128, const CUtensorMap &qmap, int num_sms,
                            cudaStream_t stream);
 
 // ---- top-k ------------------------------------------------------------------------

@@ -7,10 +7,13 @@
 //     logit[h, j] = scale * q[h, :] . c_j          (key = the whole row)
 //     o[h, :]     = sum_j softmax_j(logit[h, :]) c_j[:d]   (value = the latent part)
 //
-// Mapping onto sm_103a.  The selected rows are gathered 128 at a time by TMA
-// (tile::gather4: four rows x 128 bytes per instruction) into shared memory in the tensor
-// cores' 128-byte-swizzled layout: chunk c of a tile holds dims 64c..64c+63 of the 128
-// rows.  That one layout serves both products:
+// Mapping onto sm_103a.  The selected rows are gathered 128 at a time with cp.async
+// (16-byte granules, issued by the softmax threads while they would otherwise wait for
+// the next tile; a separate warp resolves row addresses two tiles ahead) into shared
+// memory in the tensor cores' 128-byte-swizzled layout: chunk c of a tile holds dims
+// 64c..64c+63 of the 128 rows.  (TMA gather4 issues at about one instruction per 65
+// cycles per SM, which is ~10 us per 144 KB tile; cp.async from 128 threads is far
+// cheaper to issue.)  That one layout serves both products:
 //   S^T[key, head]  = C[key, :] . Q[head, :]      A = C (K-major), B = Q (K-major)
 //   O^T[dim, head] += C[key, dim]^T P^T[key, head] A = C^T (MN-major), B = P^T (MN-major)
 // so both run as M = 128 tcgen05 MMAs (keys resp. latent dims on M, the 64 heads on N)
@@ -34,7 +37,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 192;      // warps 0-3 softmax/epilogue, 4 MMA, 5 TMA producer
+constexpr int kThreads = 192;      // warps 0-3 softmax + gather + epilogue, 4 MMA, 5 rows
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp = 5;
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = bars + 13;
     uint64_t *q_full = bars + 14;
     uint64_t *addr_ready = bars + 15;  // [2] row table of a tile written
+    uint64_t *addr_empty = bars + 17;  // [2] row table of a tile no longer needed
     volatile int *abort_flag = (volatile int *)(bars + 20);
     uint32_t *tmem_base_sm = (uint32_t *)(bars + 20) + 1;
 
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         for (int g = 0; g < ngroups; ++g) {
-            mbar_init(&full[g], 32);
+            mbar_init(&full[g], kSoftmaxThreads);
             mbar_init(&freeb[g], 1);
         }
         mbar_init(s_full, 1);
@@ -190,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         mbar_init(&addr_ready[0], 32);
         mbar_init(&addr_ready[1], 32);
+        mbar_init(&addr_empty[0], kSoftmaxThreads);
+        mbar_init(&addr_empty[1], kSoftmaxThreads);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -207,70 +213,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 64;     // nmb x 64 columns
 
     if (warp == kProducerWarp) {
-        // ================= TMA producer (lane l owns tile rows 4l .. 4l+3) ==============
-        const CUtensorMap *qmap = &maps.q[layer];
-        const CUtensorMap *kvmap = &maps.kv[layer];
+        // ===== query TMA, then the physical row of every selected key, 2 tiles ahead =====
         if (lane == 0) {
+            const CUtensorMap *qmap = &maps.q[layer];
             prefetch_tmap(qmap);
-            prefetch_tmap(kvmap);
             mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
             for (int c = 0; c < nch; ++c)
                 tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
         }
-        bool ok = true;
-        for (int li = 0; li < ntiles && ok; ++li) {
+        for (int li = 0; li < ntiles; ++li) {
             const int buf = li & 1;
+            if (li >= 2) {
+                const bool got = mbar_wait(&addr_empty[buf], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) break;
+            }
             const int j0 = (t_begin + li) * kTileKeys + lane * 4;
             int y[4];
-            int first_valid = -1;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = j0 + e;
                 int64_t r = -1;
                 if (j < p.k) {
-                    const int s = idx_row[j];
+                    const int s = __ldg(idx_row + j);
                     if (s >= 0) {
                         r = resolve_row(p.layout, b, s);
                         if (r < 0) record_error(KID_MLA, ERR_BAD_INDEX);
                     }
                 }
                 y[e] = (int)r;
-                if (r >= 0 && first_valid < 0) first_valid = (int)r;
             }
             *(int4 *)(rows_sm + buf * kTileKeys + lane * 4) = make_int4(y[0], y[1], y[2], y[3]);
             mbar_arrive(&addr_ready[buf]);
-            const bool any = first_valid >= 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (y[e] < 0) y[e] = first_valid;  // masked later; never out of range
-            for (int g = 0; g < ngroups; ++g) {
-                if (li > 0) {
-                    ok = mbar_wait(&freeb[g], (li - 1) & 1, KID_MLA, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                }
-                const bool is_rope = (g == ngroups - 1);
-                const int c0 = is_rope ? rope : 2 * g;
-                const int nck = is_rope ? 1 : min(2, nv - 2 * g);
-                const uint32_t lane_bytes = any ? (uint32_t)(nck * 4 * 128) : 0u;
-                uint32_t tot = __reduce_add_sync(0xffffffffu, lane_bytes);
-                if (lane == 0) mbar_expect_tx(&full[g], tot);
-                __syncwarp();
-                // rows 4*lane .. 4*lane+3: atom (lane / 2), half (lane & 1) of it
-                const uint32_t row_off = (uint32_t)(lane >> 1) * 1024 + (uint32_t)(lane & 1) * 512;
-                for (int c = c0; c < c0 + nck; ++c) {
-                    uint8_t *dst = tile + c * kChunkBytes + row_off;
-                    if (any) {
-                        tma_gather4(dst, kvmap, &full[g], c * 64, y[0], y[1], y[2], y[3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            *(uint4 *)(dst + e * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                if (!any) fence_proxy_async();
-                mbar_arrive(&full[g]);
-            }
         }
     } else if (warp == kMmaWarp) {
         // ================= MMA issuer =================
@@ -286,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&full[g], li & 1, KID_MLA, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
+                    fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
                     const bool is_rope = (g == ngroups - 1);
                     const int c0 = is_rope ? rope : 2 * g;
                     const int nck = is_rope ? 1 : min(2, nv - 2 * g);
@@ -329,12 +303,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         float lp[64];
 #pragma unroll
         for (int h = 0; h < 64; ++h) lp[h] = 0.f;
+        const uint16_t *kv = p.kv[layer];
+        const int D = p.d + p.r;
+        // Gather group g of tile li (its row table must be ready and the group free):
+        // thread t owns one 16-byte column of the group and every 8th (or 16th) row, so
+        // its swizzled destination advances by a constant 1 KB (or 2 KB) per step.
+        auto gather_group = [&](int li, int g) {
+            const int32_t *rows = rows_sm + (li & 1) * kTileKeys;
+            const bool is_rope = (g == ngroups - 1);
+            const int c0 = is_rope ? rope : 2 * g;
+            const int nck = is_rope ? 1 : min(2, nv - 2 * g);
+            if (nck == 2) {
+                const int gc = kl & 15, rb = kl >> 4;
+                const int c = c0 + (gc >> 3), gr = gc & 7;
+                uint8_t *dst = tile + c * kChunkBytes + rb * 128 + ((gr ^ rb) << 4);
+                const int col = c * 64 + gr * 8;
+#pragma unroll 4
+                for (int i = 0; i < 16; ++i) {
+                    const int r = rows[rb + 8 * i];
+                    cp_async_16(dst + i * 1024, r >= 0 ? kv + (int64_t)r * D + col : kv, r >= 0 ? 16u : 0u);
+                }
+            } else {
+                const int gr = kl & 7, rb = kl >> 3;  // rows rb + 16 i
+                uint8_t *dst = tile + c0 * kChunkBytes + (rb >> 3) * 1024 + (rb & 7) * 128 + ((gr ^ (rb & 7)) << 4);
+                int col = c0 * 64 + gr * 8;
+                bool in = true;
+                if (is_rope) {
+                    col = p.d + gr * 8;
+                    in = gr * 8 < p.r;
+                }
+#pragma unroll 4
+                for (int i = 0; i < 8; ++i) {
+                    const int r = rows[rb + 16 * i];
+                    const bool go = in && r >= 0;
+                    cp_async_16(dst + i * 2048, go ? kv + (int64_t)r * D + col : kv, go ? 16u : 0u);
+                }
+            }
+            cp_async_arrive(&full[g]);
+        };
         bool ok = true;
-        for (int li = 0; li < ntiles; ++li) {
+        // tile 0: every group is free
+        if (ntiles > 0) {
+            const bool got = mbar_wait(&addr_ready[0], 0, KID_MLA, abort_flag);
+            if (named_bar_or(2, kSoftmaxThreads, !got)) ok = false;
+            else
+                for (int g = 0; g < ngroups; ++g) gather_group(0, g);
+        }
+        for (int li = 0; li < ntiles && ok; ++li) {
             // every decision that guards a named barrier or a warp-collective TMEM access
             // is made uniform over the 128 threads first
-            const bool got = mbar_wait(&addr_ready[li & 1], (li >> 1) & 1, KID_MLA, abort_flag) &&
-                             mbar_wait(s_full, li & 1, KID_MLA, abort_flag);
+            const bool got = mbar_wait(s_full, li & 1, KID_MLA, abort_flag);
             if (named_bar_or(2, kSoftmaxThreads, !got)) { ok = false; break; }
             tc_fence_after();
             const bool valid = rows_sm[(li & 1) * kTileKeys + kl] >= 0;
@@ -405,7 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(p_ready);
             if (!ok) break;
+            mbar_arrive(&addr_empty[li & 1]);  // row table of tile li fully used
+            // gathers of the next tile, group by group as the O product frees them
+            if (li + 1 < ntiles) {
+                bool g_ok = mbar_wait(&addr_ready[(li + 1) & 1], ((li + 1) >> 1) & 1, KID_MLA, abort_flag);
+                if (named_bar_or(2, kSoftmaxThreads, !g_ok)) { ok = false; break; }
+                for (int g = 0; g < ngroups; ++g) {
+                    g_ok = mbar_wait(&freeb[g], li & 1, KID_MLA, abort_flag);
+                    if (named_bar_or(2, kSoftmaxThreads, !g_ok)) { ok = false; break; }
+                    gather_group(li + 1, g);
+                }
+                if (!ok) break;
+            }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         // ---- epilogue ----
         named_bar_sync(1, kSoftmaxThreads);
         if (ntiles > 0) {
