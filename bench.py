@@ -302,12 +302,8 @@ def main():
     torch.cuda.synchronize()
     layers[0].check_device_error()
 
-    # ---- timed region: K steps, per-kernel events on the launching stream -------------
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # ---- timed region: K whole steps, bracketed by a barrier and synchronize ------------
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         # untimed pre-roll of the same steps, so that the clock samples see this load
         t_stop, i = time.time() + 1.0, 0
@@ -317,19 +313,12 @@ def main():
             if i % 16 == 0:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            lay = layers[i % len(layers)]
-            ev[i][0].record(stream)
-            lay.indexer()
-            ev[i][1].record(stream)
-            lay.topk()
-            ev[i][2].record(stream)
-            if shared:
-                lay.mla_shared()
-            else:
-                lay.mla()
-            ev[i][3].record(stream)
+            step(layers[i % len(layers)])
         end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -340,10 +329,57 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    k_idx = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    k_topk = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    k_mla = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
     layers[0].check_device_error()
+
+    # ---- per-kernel durations: each call type launched K times back to back (its inputs
+    # are the previous steps' outputs), events around the loop, average per launch -----
+    def time_calls(fn):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            fn(layers[i % len(layers)])
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    k_idx = time_calls(lambda lay: lay.indexer())
+    k_topk = time_calls(lambda lay: lay.topk())
+    k_mla = time_calls(lambda lay: lay.mla_shared() if shared else lay.mla())
+
+    # ---- the same K steps replayed from a CUDA graph of the C-ABI calls ----------------
+    graph_ms = None
+    try:
+        graphs = []
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for lay in layers:
+                lay.stream = cap
+                step(lay)  # warm the per-kernel attribute set-up outside capture
+            torch.cuda.synchronize()
+            for lay in layers:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    step(lay)
+                graphs.append(g)
+        for lay in layers:
+            lay.stream = None
+        for i in range(args.warmup):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)].replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+        layers[0].check_device_error()
+    except Exception as exc:  # graphs are an extra measurement; the step time stands
+        graph_ms = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+        for lay in layers:
+            lay.stream = None
 
     b_idx, b_topk, b_mla = per_query_bytes(case)
     step_bytes = b_idx + b_topk + b_mla - scores_in_step(case)
@@ -428,6 +464,9 @@ def main():
                      "traffic": traffic_for(idx_files, "indexer"),
                      "algorithmic_bytes": b_idx, "peak_source": peak_src},
         "gpu_launches": launches_per_step * args.steps,
+        "graph_replay": (graph_ms if isinstance(graph_ms, str) else
+                         {"ms_per_step": graph_ms,
+                          "value": world * q_tokens / (graph_ms * 1e-3), "unit": UNIT}),
         "clocks": clocks.summary(),
     }
     if e2e:

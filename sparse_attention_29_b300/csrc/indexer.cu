@@ -14,12 +14,14 @@
 // The key cache streams through a TMA ring of 128-row tiles (HBM-bound for decode);
 // the query group sits in shared memory (double-buffered across groups).
 //
-// Roles (320 threads): warp 0 produces (it resolves the cache rows of 32 tiles at a time,
+// Roles (352 threads): warp 0 produces (it resolves the cache rows of 32 tiles at a time,
 // one lane per tile, then issues the TMA key loads, the query-group loads and cp.async
-// copies of the key scales into a small ring), warp 1 issues the MMAs, warps 2-9 run the
-// epilogue in two sets of four that take alternate tiles (warp w reads TMEM lanes
-// 32*(w%4) .. +31), so that every SM sub-partition has two epilogue warps to switch
-// between.  Nothing on the per-tile path waits on a global load.  CTAs are persistent: the tiles of all query groups form one list and
+// copies of the key scales into a small ring), warps 1 and 10 issue the MMAs of
+// alternate tiles (one elected thread each: the issue loop of one thread, ~1100 cycles
+// per tile, would be slower than the 16 KB per ~750 cycles an SM's share of HBM
+// delivers), warps 2-9 run the epilogue in two sets of four that take alternate tiles
+// (warp w reads TMEM lanes 32*(w%4) .. +31).  Nothing on the per-tile path waits on a
+// global load.  CTAs are persistent: the tiles of all query groups form one list and
 // each CTA takes a contiguous slice of it, so ragged contexts balance evenly.
 #include "internal.h"
 #include "ptx.cuh"
@@ -29,7 +31,8 @@ namespace {
 
 constexpr int kEpiSets = 2;                     // epilogue warp sets (alternate tiles)
 constexpr int kEpiWarps = 4 * kEpiSets;
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer + MMA + epilogue warps
+constexpr int kMmaWarps = 2;                    // MMA issuers (alternate tiles): warps 1, 10
+constexpr int kThreads = 32 * (1 + kMmaWarps + kEpiWarps);
 constexpr int kTileKeys = 128;
 constexpr int kBoxRows = 64;
 
@@ -206,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    griddep_launch_dependents();
+    griddep_wait();  // inputs may come from the previous kernel in the stream
 
     // ---- tile list: tiles of each query group, prefix-summed -------------------------
     {
@@ -262,18 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 32);  // every producer lane (lane 0 also adds the TMA bytes)
-            mbar_init(&qempty[i], 1 + kEpiWarps);  // MMA + every epilogue warp
+            mbar_init(&qempty[i], kMmaWarps + kEpiWarps);  // every MMA issuer and epilogue warp
         }
         for (int i = 0; i < p.num_acc; ++i) {
             mbar_init(&accfull[i], 1);
             mbar_init(&accempty[i], 4);
         }
         for (int i = 0; i < L.ring; ++i) mbar_init(&ksfull[i], 32);  // every producer lane
-        mbar_init(drain, 1);
+        mbar_init(drain, kMmaWarps);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == 1) {  // allocates and frees the tensor memory
         tmem_alloc(tmem_base_sm, (uint32_t)(p.acc_cols * p.num_acc));
         tmem_relinquish();
     }
@@ -287,6 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_base_sm;
 
+    const bool mma_warp = (warp == 1 || warp >= 2 + kEpiWarps);
+    const int mma_rank = warp == 1 ? 0 : warp - (1 + kEpiWarps);  // 0 .. kMmaWarps-1
     if (warp == 0) {
         // ================= producer =================
         // query group g -> slot: q codes by TMA (rows n = qi*HP + h) when the heads need no
@@ -455,8 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
+    } else if (mma_warp) {
+        // ================= MMA issuers =================
         // Per tile: stage, accumulator and phases advance by counters; the group changes
         // when the tile index reaches the next group's first tile (one compare per tile).
         if (lane == 0) {
@@ -475,19 +482,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++gcount;
                     if (!ok) break;
                 }
-                ok = mbar_wait(&kfull[stage], kphase, KID_INDEXER, abort_flag);
-                if (ok && it >= p.num_acc)
-                    ok = mbar_wait(&accempty[abuf], aphase ^ 1u, KID_INDEXER, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t a_off = (uint32_t)(stage * kTileBytes) >> 4;
-                const uint32_t b_off = (uint32_t)(qslot * L.qbuf_bytes) >> 4;
-                const uint32_t d = tmem + (uint32_t)(abuf * p.acc_cols);
+                if (it % kMmaWarps == mma_rank) {
+                    ok = mbar_wait(&kfull[stage], kphase, KID_INDEXER, abort_flag);
+                    if (ok && it >= p.num_acc)
+                        ok = mbar_wait(&accempty[abuf], aphase ^ 1u, KID_INDEXER, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a_off = (uint32_t)(stage * kTileBytes) >> 4;
+                    const uint32_t b_off = (uint32_t)(qslot * L.qbuf_bytes) >> 4;
+                    const uint32_t d = tmem + (uint32_t)(abuf * p.acc_cols);
 #pragma unroll
-                for (int ks = 0; ks < DI / 32; ++ks)
-                    mma_e4m3(d, adesc0 + a_off + 2 * ks, bdesc0 + b_off + 2 * ks, idesc, ks > 0 ? 1u : 0u);
-                mma_commit(&kempty[stage]);
-                mma_commit(&accfull[abuf]);
+                    for (int ks = 0; ks < DI / 32; ++ks)
+                        mma_e4m3(d, adesc0 + a_off + 2 * ks, bdesc0 + b_off + 2 * ks, idesc, ks > 0 ? 1u : 0u);
+                    mma_commit(&kempty[stage]);
+                    mma_commit(&accfull[abuf]);
+                }
+                // every issuer releases the query slot at the group's end (its own MMAs on
+                // that slot, if any, are covered by the commit)
                 if (gw.is_last(it)) mma_commit(&qempty[qslot]);
                 gw.step(it);
                 if (++stage == p.stages) { stage = 0; kphase ^= 1u; }
@@ -615,14 +626,12 @@ cudaError_t launch_di(const IndexerParams &p, const CUtensorMap &kmap,
     const size_t bytes = L.total + 1024;
     static int attr_set_bytes = 0;  // per process; max over calls
     if ((int)bytes > attr_set_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_kernel<DI, kW64>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes);
+        cudaError_t e = set_smem_attrs(indexer_kernel<DI, kW64>, (int)bytes);
         if (e != cudaSuccess) return e;
         attr_set_bytes = (int)bytes;
     }
-    indexer_kernel<DI, kW64><<<grid, kThreads, bytes, stream>>>(kmap, kmap128, qmap, p);
-    return cudaGetLastError();
+    return launch_pdl(indexer_kernel<DI, kW64>, dim3(grid), dim3(kThreads), bytes, stream, kmap,
+                      kmap128, qmap, p);
 }
 
 }  // namespace

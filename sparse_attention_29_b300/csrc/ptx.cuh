@@ -375,6 +375,20 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef DSA_W8
 
 // ---------------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with the programmatic-serialization
+// attribute may start while its predecessor in the stream is still running; it must call
+// griddep_wait() before it touches global memory the predecessor may write or read.
+// griddep_launch_dependents() lets the next kernel be scheduled (it still waits itself).
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------
 // misc
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }

@@ -21,6 +21,9 @@
 // tcgen05.ld a softmax thread owns one key's 64 head logits; per-head maxima are
 // reduced across the 128 keys of the tile with a transposing warp butterfly.  The
 // probabilities are written (bf16) over the tile's rope chunk, which S no longer needs.
+// One thread issues ~60-80 cycles per tcgen05.mma and a tile needs 68 of them (36 for S,
+// 32 for O), so two issuer warps split the work: each accumulates half of the S chunks
+// into its own S^T copy (the softmax adds the two) and runs half of the O M-blocks.
 // Online softmax rescales O in tensor memory only when a head's running maximum grows
 // by more than 2^8 (the result is the same; the unnormalised terms just stay < 2^8).
 // The query (64 heads x 576 x 2 B = 72 KB) and one tile (144 KB) fill shared memory,
@@ -37,9 +40,10 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 192;      // warps 0-3 softmax + gather + epilogue, 4 MMA, 5 rows
+constexpr int kThreads = 224;      // warps 0-3 softmax + gather + epilogue, 4 and 6 MMA, 5 rows
 constexpr int kSoftmaxThreads = 128;
-constexpr int kMmaWarp = 4;
+constexpr int kMmaWarp = 4;        // MMA issuer 0 (also owns the tensor memory)
+constexpr int kMmaWarp2 = 6;       // MMA issuer 1
 constexpr int kProducerWarp = 5;
 constexpr int kTileKeys = 128;
 constexpr int kHeads = 64;         // heads padded to 64 (N of both products)
@@ -122,6 +126,22 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
     tmem_ld_wait();
 }
 
+// S^T row of this thread's key: the sum of the two issuers' parts (columns 0-63, 64-127).
+__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, float (&x)[64]) {
+    uint32_t (&r)[64] = reinterpret_cast<uint32_t (&)[64]>(x);
+    tmem_ld32(taddr, reinterpret_cast<uint32_t (&)[32]>(r[0]));
+    tmem_ld32(taddr + 32, reinterpret_cast<uint32_t (&)[32]>(r[32]));
+    uint32_t y[32];
+    tmem_ld32(taddr + 64, y);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] += __uint_as_float(y[i]);
+    tmem_ld32(taddr + 96, y);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[32 + i] += __uint_as_float(y[i]);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ MlaMaps maps, const MlaParams p) {
     const int nv = p.d / 64;             // latent (value) chunks
@@ -157,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    griddep_launch_dependents();
+    griddep_wait();  // the index set comes from the previous kernel
 
     // work unit -> (row, layer, split)
     const int unit = blockIdx.x;
@@ -185,12 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int g = 0; g < ngroups; ++g) {
             mbar_init(&full[g], kSoftmaxThreads);
-            mbar_init(&freeb[g], 1);
+            mbar_init(&freeb[g], g == ngroups - 1 ? 2 : 1);  // rope/P chunk: both issuers
         }
-        mbar_init(s_full, 1);
+        mbar_init(s_full, 2);
         mbar_init(p_ready, kSoftmaxThreads);
-        mbar_init(o_done, 1);
-        mbar_init(drain, 1);
+        mbar_init(o_done, 2);
+        mbar_init(drain, 2);
         mbar_init(q_full, 1);
         mbar_init(&addr_ready[0], 32);
         mbar_init(&addr_ready[1], 32);
@@ -200,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     uint32_t tmem_cols = 32;
-    while (tmem_cols < (uint32_t)(kHeads + nmb * kHeads)) tmem_cols <<= 1;
+    while (tmem_cols < (uint32_t)(2 * kHeads + nmb * kHeads)) tmem_cols <<= 1;
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_base_sm, tmem_cols);
         tmem_relinquish();
@@ -209,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_sm;
-    const uint32_t tS = tmem;          // 64 columns
-    const uint32_t tO = tmem + 64;     // nmb x 64 columns
+    const uint32_t tS = tmem;          // 2 x 64 columns: one S^T part per MMA issuer
+    const uint32_t tO = tmem + 128;    // nmb x 64 columns
 
     if (warp == kProducerWarp) {
         // ===== query TMA, then the physical row of every selected key, 2 tiles ahead =====
@@ -245,32 +267,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             *(int4 *)(rows_sm + buf * kTileKeys + lane * 4) = make_int4(y[0], y[1], y[2], y[3]);
             mbar_arrive(&addr_ready[buf]);
         }
-    } else if (warp == kMmaWarp) {
-        // ================= MMA issuer =================
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ================= MMA issuers =================
+        // issuer r: S chunks [c_lo, c_hi) into its own S^T copy, O M-blocks [m_lo, m_hi)
+        const int r = warp == kMmaWarp ? 0 : 1;
+        const int nch_a = (nch + 1) / 2, nmb_a = (nmb + 1) / 2;
+        const int c_lo = r == 0 ? 0 : nch_a, c_hi = r == 0 ? nch_a : nch;
+        const int m_lo = r == 0 ? 0 : nmb_a, m_hi = r == 0 ? nmb_a : nmb;
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, kHeads, false, false);
             const uint32_t idO = idesc_bf16(128, kHeads, true, true);
             const uint32_t tile_a = smem_u32(tile), q_a = smem_u32(qs), p_a = smem_u32(pslot);
+            const uint32_t tSr = tS + (uint32_t)(r * kHeads);
             bool ok = ntiles == 0 || mbar_wait(q_full, 0, KID_MLA, abort_flag);
             for (int li = 0; li < ntiles && ok; ++li) {
-                // S^T = C . Q^T over all chunks, group by group as the gathers land
-                bool first = true;
-                for (int g = 0; g < ngroups && ok; ++g) {
-                    ok = mbar_wait(&full[g], li & 1, KID_MLA, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
-                    const bool is_rope = (g == ngroups - 1);
-                    const int c0 = is_rope ? rope : 2 * g;
-                    const int nck = is_rope ? 1 : min(2, nv - 2 * g);
-                    for (int c = c0; c < c0 + nck; ++c) {
+                // S^T part = C . Q^T over this issuer's chunks, as their gather groups land
+                int waited = -1;
+                for (int c = c_lo; c < c_hi && ok; ++c) {
+                    const int g = c == rope ? ngroups - 1 : c / 2;
+                    if (g != waited) {
+                        ok = mbar_wait(&full[g], li & 1, KID_MLA, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
+                        waited = g;
+                    }
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
-                            const uint64_t bd = make_sdesc(q_a + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
-                            mma_bf16(tS, ad, bd, idS, first ? 0u : 1u);
-                            first = false;
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
+                        const uint64_t bd = make_sdesc(q_a + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
+                        mma_bf16(tSr, ad, bd, idS, (c > c_lo || kk > 0) ? 1u : 0u);
                     }
                 }
                 if (!ok) break;
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O^T += C^T . P^T once the probabilities are in place
                 if (!mbar_wait(p_ready, li & 1, KID_MLA, abort_flag)) break;
                 tc_fence_after();
-                for (int j = 0; j < nmb; ++j) {
+                for (int j = m_lo; j < m_hi; ++j) {
 #pragma unroll
                     for (int ks = 0; ks < kTileKeys / 16; ++ks) {
                         const uint64_t ad = make_sdesc(tile_a + 2 * j * kChunkBytes + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
@@ -357,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool valid = rows_sm[(li & 1) * kTileKeys + kl] >= 0;
             float x[64];
-            tmem_ld64(tS + lane_addr, x);
+            tmem_ld_s(tS + lane_addr, x);
 #pragma unroll
             for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
             warp_transpose_reduce<true>(x, lane);
@@ -375,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool any = named_bar_or(2, kSoftmaxThreads, need);
             // probabilities of this key for every head
-            tmem_ld64(tS + lane_addr, x);
+            tmem_ld_s(tS + lane_addr, x);
             uint32_t pk[32];
 #pragma unroll
             for (int h = 0; h < 64; h += 2) {
@@ -524,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const MlaParams p) {
+    griddep_launch_dependents();
+    griddep_wait();  // the partials come from the previous kernel
     const int h = blockIdx.x % kHeads;
     const int unit = blockIdx.x / kHeads;  // row * layers + layer
     if (h >= p.H) return;
@@ -589,19 +617,16 @@ cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStrea
     const size_t bytes = L.total + 1024;
     static int attr_bytes = 0;
     if ((int)bytes > attr_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes);
+        cudaError_t e = set_smem_attrs(sparse_mla_kernel, (int)bytes);
         if (e != cudaSuccess) return e;
         attr_bytes = (int)bytes;
     }
     const int units = p.B * p.T * p.layers;
     if (units <= 0) return cudaSuccess;
-    sparse_mla_kernel<<<units * p.splits, kThreads, bytes, stream>>>(maps, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(sparse_mla_kernel, dim3(units * p.splits), dim3(kThreads), bytes,
+                               stream, maps, p);
     if (e != cudaSuccess || p.splits == 1) return e;
-    mla_combine_kernel<<<units * kHeads, kCombineThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(mla_combine_kernel, dim3(units * kHeads), dim3(kCombineThreads), 0, stream, p);
 }
 
 DSA_DEFINE_ERROR_READER(take_error_mla)

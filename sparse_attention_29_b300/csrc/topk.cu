@@ -103,6 +103,8 @@ __device__ __forceinline__ void find_crossing(TopkSmem &sm, uint32_t r) {
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     TopkSmem &sm = *reinterpret_cast<TopkSmem *>(smem_raw);
+    griddep_launch_dependents();
+    griddep_wait();  // the scores come from the previous kernel
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
     const int k = p.k;
@@ -252,15 +254,12 @@ cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream) {
     const size_t bytes = sizeof(TopkSmem);
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes);
+        cudaError_t e = set_smem_attrs(topk_kernel, (int)bytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     if (p.rows <= 0) return cudaSuccess;
-    topk_kernel<<<p.rows, kThreads, bytes, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3(p.rows), dim3(kThreads), bytes, stream, p);
 }
 
 DSA_DEFINE_ERROR_READER(take_error_topk)
