@@ -332,15 +332,41 @@ def main():
     layers[0].check_device_error()
 
     # ---- per-kernel durations: each call type launched K times back to back (its inputs
-    # are the previous steps' outputs), events around the loop, average per launch -----
+    # are the previous steps' outputs), captured into one CUDA graph and replayed, so that
+    # the host's per-call submission cost does not read as device time; events on the
+    # launching stream around the replay, average per launch --------------------------
     def time_calls(fn):
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(args.steps):
-            fn(layers[i % len(layers)])
-        b.record(stream)
-        torch.cuda.synchronize()
+        try:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                for lay in layers:
+                    lay.stream = cap
+                fn(layers[0])
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    for i in range(args.steps):
+                        fn(layers[i % len(layers)])
+            for lay in layers:
+                lay.stream = None
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+        except Exception:  # no capture: an eager loop (includes host submission time)
+            for lay in layers:
+                lay.stream = None
+            torch.cuda.synchronize()
+            a.record(stream)
+            for i in range(args.steps):
+                fn(layers[i % len(layers)])
+            b.record(stream)
+            torch.cuda.synchronize()
         return a.elapsed_time(b) / args.steps
 
     k_idx = time_calls(lambda lay: lay.indexer())

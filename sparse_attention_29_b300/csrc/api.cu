@@ -258,7 +258,9 @@ dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int L
     p.rows = rows;
     p.Lmax = Lmax;
     p.k = k;
-    return from_cuda(launch_topk(p, static_cast<cudaStream_t>(stream)));
+    const int sms = current_sm_count();
+    if (sms <= 0) return DSA_ERR_CUDA;
+    return from_cuda(launch_topk(p, sms, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,

@@ -88,7 +88,7 @@ struct TopkParams {
     int rows, Lmax, k;
 };
 
-cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream);
+cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream);
 
 // ---- sparse MLA -------------------------------------------------------------------
 constexpr int kMaxLayers = 8;

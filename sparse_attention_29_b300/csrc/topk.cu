@@ -1,23 +1,25 @@
-// topk.cu -- causal top-k selection with the dense fallback, one CTA per query row.
+// topk.cu -- causal top-k selection with the dense fallback.
 //
 // Source: "Inside GLM-5.3: How Sparse Attention Affects DRAM Memory TAM", §Lightning
 // Indexer (keep the top-K tokens by indexer score; a query that attends fewer than K
 // tokens stays dense) and §Sparse MLA (K = 2048).  Equal scores go to the lower token
 // index, so the selection is deterministic; indices are written in ascending order.
 //
-// Method: radix select on order-preserving integer keys of the fp32 scores.
-//   1. coarse pass: a 2048-bin histogram of an 11-bit key taken from the score rounded to
-//      fp16 (sign, 5 exponent bits, 5 mantissa bits).  Rounding to fp16 is monotone, so
-//      the bins are ordered like the scores, and 32 bins per octave spread a realistic
-//      score distribution far better than the top bits of the fp32 pattern would.  The
-//      bin holding the k-th largest score is found by a suffix count.
-//   2. refine: inside that bin only, three radix passes (11, 11, 10 bits) over the full
-//      32-bit key find the k-th largest key T exactly, and how many elements equal to T
-//      must still be taken.
-//   3. one ordered pass writes every element above T and the lowest-index elements equal
-//      to T, in ascending index order (block-wide prefix sums).
-// Rows of up to 40960 candidates are staged in shared memory once; longer rows are read
-// again from global memory (L2) by each pass.
+// One thread-block cluster per query row; CTA r of the cluster owns a contiguous slice
+// of the row's candidates and keeps it in shared memory.  Keys are order-preserving
+// integer images of the fp32 scores.
+//   1. coarse: every CTA histograms an 11-bit key of its slice (the score rounded to
+//      fp16: sign, 5 exponent and 5 mantissa bits -- monotone, and 32 bins per octave
+//      spread realistic scores far better than the top bits of the fp32 pattern).  The
+//      cluster sums the histograms through distributed shared memory and every CTA finds
+//      the bin B0 that holds the k-th largest score, and how many it still needs from B0.
+//   2. exact: the B0 candidates of all slices (typically a few hundred) are ranked by
+//      (score, then lower index) by direct comparison; with more than kCandCap of them
+//      (many exact ties) three distributed radix passes over the full 32-bit keys find
+//      the k-th key instead, and ties are taken lowest index first across the slices.
+//   3. output: CTAs exchange how many they select; each writes its selections, in index
+//      order, at its offset.
+// Rows that see at most k tokens skip all of this and write 0..n-1 then -1 padding.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -26,12 +28,11 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCacheCap = 40960;
-constexpr int kCandCap = 4096;
 constexpr int kBins = 2048;
-constexpr int kItems = 8;  // consecutive elements per thread in the ordered pass
+constexpr int kCandCap = 2048;  // candidates ranked directly (per row, all slices)
+constexpr int kMaxCluster = 8;
 
 // Order-preserving map fp32 -> uint32 (larger score -> larger key); -0 and +0 are one key.
 __device__ __forceinline__ uint32_t full_key(float f) {
@@ -48,15 +49,81 @@ __device__ __forceinline__ uint32_t coarse_key(float f) {
     return u >> 5;
 }
 
-struct TopkSmem {
-    float cache[kCacheCap];
-    uint32_t hist[kBins];
-    uint32_t cand_key[kCandCap];
+// ---- cluster primitives -------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a 32-bit word at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_ld(const void *local_ptr, uint32_t rank) {
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Read four consecutive 32-bit words (16-byte aligned) from CTA `rank` of the cluster.
+__device__ __forceinline__ uint4 dsmem_ld4(const void *local_ptr, uint32_t rank) {
+    uint32_t remote;
+    uint4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
+// ---- shared memory --------------------------------------------------------------------
+
+struct Ctrl {
+    uint64_t load_bar;
     uint32_t warp_tot[kWarps];
-    uint32_t cand_count;
+    uint32_t warp_st[kWarps], warp_eq[kWarps];  // per-warp counts (ordered pass)
     int found_bin;
     uint32_t found_above;
+    uint32_t n_cand;      // B0 candidates in this slice (read by peers)
+    uint32_t n_strict;    // surely selected in this slice (read by peers)
+    uint32_t n_eq;        // keys equal to the threshold in this slice (read by peers)
 };
+
+struct Layout {
+    uint32_t vals, bitmap, masks, cand_key, cand_idx, hist, tot, ctrl, total;
+};
+
+__host__ __device__ inline Layout topk_layout(int slice_cap) {
+    Layout L;
+    uint32_t off = 0;
+    L.vals = off;  // the slice starts at its global 16-byte phase: up to 3 floats in
+    off += ((uint32_t)slice_cap + 4) * 4;
+    L.bitmap = off;
+    off += ((uint32_t)slice_cap + 31) / 32 * 4;
+    off = (off + 15) & ~15u;
+    L.masks = off;  // two ballots per 32 elements
+    off += ((uint32_t)slice_cap + 31) / 32 * 8 + 16 * 8;
+    off = (off + 15) & ~15u;
+    L.cand_key = off;
+    off += kCandCap * 4;
+    L.cand_idx = off;
+    off += kCandCap * 4;
+    L.hist = off;
+    off += 2 * kBins * 4;
+    L.tot = off;
+    off += kBins * 4;
+    L.ctrl = off;
+    off += sizeof(Ctrl);
+    L.total = (off + 15) & ~15u;
+    return L;
+}
 
 // Block-wide exclusive scan of one uint32 per thread (all threads must call it).
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tot) {
@@ -70,196 +137,405 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
     if (lane == 31) warp_tot[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        const uint32_t t = warp_tot[lane];
+        const uint32_t t = lane < kWarps ? warp_tot[lane] : 0u;
         uint32_t s = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
             if (lane >= o) s += y;
         }
-        warp_tot[lane] = s - t;  // exclusive prefix of the warp totals
+        if (lane < kWarps) warp_tot[lane] = s - t;
     }
     __syncthreads();
-    return warp_tot[warp] + x - v;
+    const uint32_t res = warp_tot[warp] + x - v;
+    __syncthreads();  // warp_tot is reused by the next call
+    return res;
 }
 
-// Find the bin holding the r-th largest element (1-based r) of hist[0..kBins): sets
-// sm.found_bin and sm.found_above = count of elements in higher bins.
-__device__ __forceinline__ void find_crossing(TopkSmem &sm, uint32_t r) {
-    const int t = threadIdx.x;
-    const int b_hi = kBins - 1 - 2 * t;  // this thread's bins, descending: b_hi, b_hi - 1
-    const uint32_t c0 = sm.hist[b_hi], c1 = sm.hist[b_hi - 1];
-    const uint32_t above = block_excl_scan(c0 + c1, sm.warp_tot);
-    if (above < r && above + c0 >= r) {
-        sm.found_bin = b_hi;
-        sm.found_above = above;
-    } else if (above + c0 < r && above + c0 + c1 >= r) {
-        sm.found_bin = b_hi - 1;
-        sm.found_above = above + c0;
+// Sum the cluster's histograms (`hist`, at the same offset in every CTA) into tot and
+// find the bin holding the r-th largest element (1-based): sets c.found_bin and
+// c.found_above (elements in higher bins).  Thread t owns the four bins of group
+// kThreads-1-t, so a block scan in thread order walks the bins in descending order.
+static_assert(kBins == 4 * kThreads, "four bins per thread");
+__device__ __forceinline__ void cluster_crossing(const uint32_t *hist, uint32_t *tot, int csize,
+                                                 Ctrl &c, uint32_t r) {
+    const int g = kThreads - 1 - (int)threadIdx.x;
+    uint4 s = reinterpret_cast<const uint4 *>(hist)[g];
+    if (csize > 1) {
+        s = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int rr = 0; rr < kMaxCluster; ++rr) {
+            if (rr < csize) {
+                const uint4 v = dsmem_ld4(hist + 4 * g, (uint32_t)rr);
+                s.x += v.x;
+                s.y += v.y;
+                s.z += v.z;
+                s.w += v.w;
+            }
+        }
+    }
+    reinterpret_cast<uint4 *>(tot)[g] = s;
+    const uint32_t cnt[4] = {s.w, s.z, s.y, s.x};  // bins 4g+3 down to 4g
+    uint32_t above = block_excl_scan(s.x + s.y + s.z + s.w, c.warp_tot);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (above < r && above + cnt[i] >= r) {
+            c.found_bin = 4 * g + 3 - i;
+            c.found_above = above;
+        }
+        above += cnt[i];
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    TopkSmem &sm = *reinterpret_cast<TopkSmem *>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, int csize,
+                                                            int slice_cap) {
     griddep_launch_dependents();
     griddep_wait();  // the scores come from the previous kernel
-    const int row = blockIdx.x;
+
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const Layout Ly = topk_layout(slice_cap);
+    float *vals = reinterpret_cast<float *>(smem_raw + Ly.vals);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem_raw + Ly.bitmap);
+    uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + Ly.cand_key);
+    int32_t *cand_idx = reinterpret_cast<int32_t *>(smem_raw + Ly.cand_idx);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem_raw + Ly.hist);  // [2][kBins]
+    uint32_t *tot = reinterpret_cast<uint32_t *>(smem_raw + Ly.tot);
+    Ctrl &ctrl = *reinterpret_cast<Ctrl *>(smem_raw + Ly.ctrl);
+
     const int tid = threadIdx.x;
+    const int row = blockIdx.x / csize;
+    const uint32_t rank = csize > 1 ? cluster_rank() : 0u;
     const int k = p.k;
     int32_t *out = p.idx + (int64_t)row * k;
     int n = p.q_pos[row] + 1;
     if (n < 1 || n > p.Lmax) {
-        if (tid == 0) record_error(KID_TOPK, ERR_BAD_POSITION);
+        if (tid == 0 && rank == 0) record_error(KID_TOPK, ERR_BAD_POSITION);
         n = n < 1 ? 0 : p.Lmax;
     }
-    if (n <= k) {  // dense: every visible token, then padding
-        for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    if (n <= k) {  // dense: every visible token, then padding (uniform for the cluster)
+        const int per = (k + csize - 1) / csize;
+        const int lo = (int)rank * per, hi = min(k, lo + per);
+        for (int i = lo + tid; i < hi; i += kThreads) out[i] = i < n ? i : -1;
         return;
     }
-    const float *src = p.scores + (int64_t)row * p.Lmax;
-    const bool cached = n <= kCacheCap;
-    if (cached) {
-        if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-            const int n4 = n >> 2;
-            for (int i = tid; i < n4; i += kThreads)
-                reinterpret_cast<float4 *>(sm.cache)[i] = __ldg(reinterpret_cast<const float4 *>(src) + i);
-            for (int i = (n4 << 2) + tid; i < n; i += kThreads) sm.cache[i] = __ldg(src + i);
-        } else {
-            for (int i = tid; i < n; i += kThreads) sm.cache[i] = __ldg(src + i);
+
+    // ---- this CTA's slice [s_lo, s_hi) of the row, staged in shared memory ------------
+    const int per = (n + csize - 1) / csize;
+    const int s_lo = min(n, (int)rank * per), s_hi = min(n, s_lo + per);
+    const int m = s_hi - s_lo;
+    const float *src = p.scores + (int64_t)row * p.Lmax + s_lo;
+    {
+        // the 16-byte-aligned middle of the slice by bulk asynchronous copies (the slice
+        // in shared memory starts at the same alignment phase), the ends by plain loads
+        const int head = min(m, (int)(((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15) / 4));
+        const int mid = ((m - head) >> 2) << 2;
+        float *dst = vals + ((reinterpret_cast<uintptr_t>(src) & 15) >> 2);  // same phase
+        if (tid == 0) {
+            mbar_init(&ctrl.load_bar, 1);
+            fence_barrier_init();
         }
+        __syncthreads();
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&ctrl.load_bar, (uint32_t)mid * 4);
+            for (int off = 0; off < mid; off += 8192) {
+                const int len = min(8192, mid - off);
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        smem_u32(dst + head + off)),
+                    "l"(src + head + off), "r"(len * 4), "r"(smem_u32(&ctrl.load_bar))
+                    : "memory");
+            }
+        }
+        for (int i = tid; i < head; i += kThreads) dst[i] = __ldg(src + i);
+        for (int i = head + mid + tid; i < m; i += kThreads) dst[i] = __ldg(src + i);
+        for (int b = tid; b < 2 * kBins; b += kThreads) hist[b] = 0;
+        for (int w = tid; w < (m + 31) / 32; w += kThreads) bitmap[w] = 0;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&ctrl.load_bar, 0)) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                record_error(KID_TOPK, ERR_WAIT_TIMEOUT);
+                break;
+            }
+        }
+        vals = dst;
     }
-    auto score = [&](int i) -> float { return cached ? sm.cache[i] : __ldg(src + i); };
+    __syncthreads();
+    // warp w owns the contiguous segment [w_lo, w_hi) of the slice and walks it in steps of
+    // 32 consecutive elements (lane l takes element 32j + l): ballots give each step's
+    // hits in index order without bank conflicts or atomics
+    const int lane = tid & 31, warp = tid >> 5;
+    const int seg = ((m + kWarps - 1) / kWarps + 31) & ~31;
+    const int w_lo = min(m, warp * seg), w_hi = min(m, w_lo + seg);
+    uint32_t *wmask = reinterpret_cast<uint32_t *>(smem_raw + Ly.masks) + 2 * (w_lo >> 5);
 
-    // ---- 1. coarse histogram ---------------------------------------------------------
-    for (int b = tid; b < kBins; b += kThreads) sm.hist[b] = 0;
-    if (tid == 0) sm.cand_count = 0;
+    // ---- 1. coarse histogram, summed over the cluster -------------------------------
+#pragma unroll 4
+    for (int i = tid; i < m; i += kThreads) atomicAdd(&hist[coarse_key(vals[i])], 1u);
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) atomicAdd(&sm.hist[coarse_key(score(i))], 1u);
-    __syncthreads();
-    find_crossing(sm, (uint32_t)k);
-    const uint32_t B0 = (uint32_t)sm.found_bin;
-    uint32_t r = (uint32_t)k - sm.found_above;  // still to take from bin B0
-    const uint32_t c0 = sm.hist[B0];
-    __syncthreads();
+    if (csize > 1) cluster_sync();
+    cluster_crossing(hist, tot, csize, ctrl, (uint32_t)k);
+    const uint32_t B0 = (uint32_t)ctrl.found_bin;
+    const uint32_t r0 = (uint32_t)k - ctrl.found_above;  // still needed from bin B0
+    const uint32_t c0 = tot[B0];                          // B0 elements in the row
 
-    // ---- 2. exact threshold inside bin B0 ---------------------------------------------
-    bool all_bin = (r == c0);
-    uint32_t T = 0;
-    if (!all_bin) {
-        const bool use_cand = c0 <= (uint32_t)kCandCap;
-        if (use_cand) {
-            for (int i = tid; i < n; i += kThreads) {
-                const float f = score(i);
-                if (coarse_key(f) == B0) {
-                    const uint32_t slot = atomicAdd(&sm.cand_count, 1u);
-                    sm.cand_key[slot] = full_key(f);
+    // ---- 2. exact selection inside B0 -------------------------------------------------
+    // afterwards: selected = coarse > B0, or coarse == B0 and
+    //   (rank path)  the element's bitmap bit is set;
+    //   (radix path) key > T, or key == T and among the first r_eq such keys of the row.
+    const bool all_bin = (r0 == c0);
+    const bool rank_path = !all_bin && c0 <= (uint32_t)kCandCap;
+    uint32_t T = 0, r_eq = 0;
+    if (rank_path) {
+        // this slice's B0 candidates, in index order: ballots, per-warp counts, then writes
+        uint32_t nc = 0;
+#pragma unroll 4
+        for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
+            const int i = w_lo + 32 * j + lane;
+            const bool is_c = i < w_hi && coarse_key(vals[i]) == B0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, is_c);
+            if (lane == 0) wmask[2 * j] = bal;
+            nc += __popc(bal);
+        }
+        if (lane == 0) ctrl.warp_st[warp] = nc;
+        __syncthreads();
+        uint32_t slot = 0, mine = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t c = ctrl.warp_st[w];
+            slot += w < warp ? c : 0u;
+            mine += c;
+        }
+        for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
+            const uint32_t bal = wmask[2 * j];
+            if ((bal >> lane) & 1u) {
+                const int i = w_lo + 32 * j + lane;
+                const uint32_t at = slot + __popc(bal & ((1u << lane) - 1u));
+                cand_key[at] = full_key(vals[i]);
+                cand_idx[at] = s_lo + i;
+            }
+            slot += __popc(bal);
+        }
+        if (tid == 0) ctrl.n_cand = mine;
+        __syncthreads();
+        if (csize > 1) cluster_sync();  // every slice's list is complete
+        // gather every slice's candidates (tot and hist are free again)
+        uint32_t *all_key = tot;                                   // kCandCap entries
+        int32_t *all_idx = reinterpret_cast<int32_t *>(hist);      // kCandCap entries
+        uint32_t total = mine;
+        if (csize > 1) {
+            uint32_t offs[kMaxCluster + 1];
+            offs[0] = 0;
+#pragma unroll
+            for (int rr = 0; rr < kMaxCluster; ++rr)
+                offs[rr + 1] = offs[rr] + (rr < csize ? dsmem_ld(&ctrl.n_cand, (uint32_t)rr) : 0u);
+            total = offs[kMaxCluster];
+            for (uint32_t j = tid; j < total; j += kThreads) {
+                uint32_t rr = 0, base = 0;
+#pragma unroll
+                for (int q = 1; q < kMaxCluster; ++q)
+                    if (j >= offs[q]) {
+                        rr = (uint32_t)q;
+                        base = offs[q];
+                    }
+                all_key[j] = dsmem_ld(cand_key + (j - base), rr);
+                all_idx[j] = (int32_t)dsmem_ld(cand_idx + (j - base), rr);
+            }
+        } else {
+            for (uint32_t j = tid; j < total; j += kThreads) {
+                all_key[j] = cand_key[j];
+                all_idx[j] = cand_idx[j];
+            }
+        }
+        __syncthreads();
+        // rank this slice's candidates against every candidate of the row: one warp per
+        // candidate, its lanes splitting the comparisons
+        {
+            for (uint32_t c = warp; c < mine; c += kWarps) {
+                const uint32_t key = cand_key[c];
+                const int32_t idx = cand_idx[c];
+                uint32_t better = 0;
+                for (uint32_t j = lane; j < total; j += 32) {
+                    const uint32_t kj = all_key[j];
+                    better += (kj > key) || (kj == key && all_idx[j] < idx);
+                }
+                better = __reduce_add_sync(0xffffffffu, better);
+                if (lane == 0 && better < r0) {
+                    const int li = idx - s_lo;
+                    atomicOr(&bitmap[li >> 5], 1u << (li & 31));
                 }
             }
-            __syncthreads();
         }
-        const int nc = use_cand ? (int)c0 : n;
-        uint32_t pref = 0;  // key bits fixed so far
-        const int shifts[3] = {21, 10, 0};
-        const uint32_t masks[3] = {0x7FFu, 0x7FFu, 0x3FFu};
+        __syncthreads();
+    } else if (!all_bin) {
+        // many exact ties: three radix passes (11, 11, 10 bits) over the full keys of B0,
+        // histograms alternating between two buffers so that one cluster barrier per pass
+        // separates a buffer's writes from its peers' reads
+        uint32_t r = r0, pref = 0;
 #pragma unroll 1
         for (int pass = 0; pass < 3; ++pass) {
-            const int sh = shifts[pass];
-            for (int b = tid; b < kBins; b += kThreads) sm.hist[b] = 0;
+            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const uint32_t mask = pass == 2 ? 0x3FFu : 0x7FFu;
+            const int hsh = pass == 0 ? 32 : (pass == 1 ? 21 : 10);
+            uint32_t *h = hist + ((pass + 1) & 1) * kBins;  // buffer 0 held the coarse pass
+            for (int b = tid; b < kBins; b += kThreads) h[b] = 0;
             __syncthreads();
-            const int hsh = pass == 0 ? 32 : shifts[pass - 1];  // bits above this digit
-            for (int i = tid; i < nc; i += kThreads) {
-                uint32_t u;
-                if (use_cand) {
-                    u = sm.cand_key[i];
-                } else {
-                    const float f = score(i);
-                    if (coarse_key(f) != B0) continue;
-                    u = full_key(f);
-                }
+            for (int i = tid; i < m; i += kThreads) {
+                const float f = vals[i];
+                if (coarse_key(f) != B0) continue;
+                const uint32_t u = full_key(f);
                 if (hsh < 32 && (u >> hsh) != (pref >> hsh)) continue;
-                atomicAdd(&sm.hist[(u >> sh) & masks[pass]], 1u);
+                atomicAdd(&h[(u >> sh) & mask], 1u);
             }
             __syncthreads();
-            find_crossing(sm, r);
-            pref |= ((uint32_t)sm.found_bin) << sh;
-            r -= sm.found_above;
-            __syncthreads();
+            if (csize > 1) cluster_sync();
+            cluster_crossing(h, tot, csize, ctrl, r);
+            pref |= ((uint32_t)ctrl.found_bin) << sh;
+            r -= ctrl.found_above;
         }
-        T = pref;  // the k-th largest key; r = how many keys equal to T to take
+        T = pref;
+        r_eq = r;
     }
 
-    // ---- 3. ordered write --------------------------------------------------------------
-    uint32_t sel_base = 0, eq_base = 0;
-    const uint32_t r_eq = r;
-    for (int base = 0; base < n; base += kThreads * kItems) {
-        const int i0 = base + tid * kItems;
-        uint32_t strict_mask = 0, eq_mask = 0;
-#pragma unroll
-        for (int e = 0; e < kItems; ++e) {
-            const int i = i0 + e;
-            if (i < n) {
-                const float f = score(i);
-                const uint32_t ck = coarse_key(f);
-                if (ck > B0) {
-                    strict_mask |= 1u << e;
-                } else if (ck == B0) {
-                    if (all_bin) {
-                        strict_mask |= 1u << e;
-                    } else {
-                        const uint32_t u = full_key(f);
-                        if (u > T) strict_mask |= 1u << e;
-                        else if (u == T) eq_mask |= 1u << e;
-                    }
-                }
+    // ---- 3. counts, offsets, ordered write --------------------------------------------
+    auto classify = [&](int i, bool &strict, bool &eq) {
+        const float f = vals[i];
+        const uint32_t ck = coarse_key(f);
+        strict = false;
+        eq = false;
+        if (ck > B0) {
+            strict = true;
+        } else if (ck == B0) {
+            if (all_bin) {
+                strict = true;
+            } else if (rank_path) {
+                strict = (bitmap[i >> 5] >> (i & 31)) & 1u;
+            } else {
+                const uint32_t u = full_key(f);
+                if (u > T) strict = true;
+                else if (u == T) eq = true;
             }
         }
-        const uint32_t eq_before = eq_base + block_excl_scan(__popc(eq_mask), sm.warp_tot);
-        // the first r_eq equal keys in index order are taken
-        uint32_t take_eq = 0, seen = eq_before;
-#pragma unroll
-        for (int e = 0; e < kItems; ++e) {
-            if (eq_mask & (1u << e)) {
-                if (seen < r_eq) take_eq |= 1u << e;
-                ++seen;
-            }
+    };
+    // per warp segment: selection ballots (strict, equal to the threshold) in index order
+    uint32_t w_st = 0, w_eq = 0;
+#pragma unroll 4
+    for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
+        const int i = w_lo + 32 * j + lane;
+        bool st = false, eq = false;
+        if (i < w_hi) classify(i, st, eq);
+        const uint32_t bst = __ballot_sync(0xffffffffu, st), beq = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) {
+            wmask[2 * j] = bst;
+            wmask[2 * j + 1] = beq;
         }
-        const uint32_t sel_mask = strict_mask | take_eq;
-        uint32_t pos = sel_base + block_excl_scan(__popc(sel_mask), sm.warp_tot);
-#pragma unroll
-        for (int e = 0; e < kItems; ++e) {
-            if (sel_mask & (1u << e)) {
-                if (pos < (uint32_t)k) out[pos] = i0 + e;
-                ++pos;
-            }
-        }
-        // chunk totals: the last thread's end position
-        __shared__ uint32_t chunk_end[2];
-        if (tid == kThreads - 1) {
-            chunk_end[0] = pos;
-            chunk_end[1] = seen;
-        }
-        __syncthreads();
-        sel_base = chunk_end[0];
-        eq_base = chunk_end[1];
-        __syncthreads();
+        w_st += __popc(bst);
+        w_eq += __popc(beq);
     }
-    if (tid == 0 && sel_base != (uint32_t)k) record_error(KID_TOPK, ERR_BAD_INDEX);
+    if (lane == 0) {
+        ctrl.warp_st[warp] = w_st;
+        ctrl.warp_eq[warp] = w_eq;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t a = 0, b = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            a += ctrl.warp_st[w];
+            b += ctrl.warp_eq[w];
+        }
+        ctrl.n_strict = a;
+        ctrl.n_eq = b;
+    }
+    __syncthreads();
+    if (csize > 1) cluster_sync();
+    // earlier slices' selections come first; equal keys are taken by ascending index
+    uint32_t sel_before = 0, eq_before = 0;
+    for (uint32_t rr = 0; rr < rank; ++rr) {
+        const uint32_t s_r = dsmem_ld(&ctrl.n_strict, rr);
+        const uint32_t e_r = dsmem_ld(&ctrl.n_eq, rr);
+        const uint32_t take = eq_before >= r_eq ? 0u : min(e_r, r_eq - eq_before);
+        sel_before += s_r + take;
+        eq_before += e_r;
+    }
+    if (csize > 1) cluster_sync();  // no CTA leaves while a peer still reads its counters
+    // this warp's offsets: earlier warps' strict selections and taken equal keys
+    uint32_t pos = sel_before, eq_seen = eq_before;
+    for (int w = 0; w < warp; ++w) {
+        const uint32_t e_w = ctrl.warp_eq[w];
+        const uint32_t take = eq_seen >= r_eq ? 0u : min(e_w, r_eq - eq_seen);
+        pos += ctrl.warp_st[w] + take;
+        eq_seen += e_w;
+    }
+    for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
+        const uint32_t bst = wmask[2 * j], beq = wmask[2 * j + 1];
+        uint32_t take = 0;
+        if (beq) {
+            const uint32_t want = eq_seen >= r_eq ? 0u : r_eq - eq_seen;
+            const uint32_t have = __popc(beq);
+            if (want >= have) {
+                take = beq;
+            } else if (want > 0) {
+                const uint32_t cut = __fns(beq, 0, (int)want + 1);  // position of the next one
+                take = beq & ((1u << cut) - 1u);
+            }
+            eq_seen += have;
+        }
+        const uint32_t sel = bst | take;
+        if ((sel >> lane) & 1u) {
+            const uint32_t at = pos + __popc(sel & ((1u << lane) - 1u));
+            if (at < (uint32_t)k) out[at] = s_lo + w_lo + 32 * j + lane;
+        }
+        pos += __popc(sel);
+    }
+    // the last warp of the last slice ends at k
+    uint32_t sel_base = pos;
+    sel_base = __shfl_sync(0xffffffffu, sel_base, 0);
+    if (warp != kWarps - 1) sel_base = (uint32_t)k;
+    if (rank == (uint32_t)csize - 1 && warp == kWarps - 1 && lane == 0 && sel_base != (uint32_t)k)
+        record_error(KID_TOPK, ERR_BAD_INDEX);
 }
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkParams &p, cudaStream_t stream) {
-    const size_t bytes = sizeof(TopkSmem);
-    static bool attr = false;
-    if (!attr) {
+// Cluster size and slice capacity of a launch: enough CTAs per row to fill the GPU when
+// rows are few, and to keep every slice within shared memory.
+static void topk_shape(const TopkParams &p, int num_sms, int &csize, int &slice_cap) {
+    constexpr int kSliceMax = 40960;
+    const int by_fill = p.rows > 0 ? num_sms / p.rows : 1;
+    const int by_size = (p.Lmax + kSliceMax - 1) / kSliceMax;
+    csize = by_fill > by_size ? by_fill : by_size;
+    if (csize < 1) csize = 1;
+    if (csize > kMaxCluster) csize = kMaxCluster;
+    slice_cap = (p.Lmax + csize - 1) / csize;
+    slice_cap = (slice_cap + 31) & ~31;
+}
+
+cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream) {
+    if (p.rows <= 0) return cudaSuccess;
+    int csize, slice_cap;
+    topk_shape(p, num_sms, csize, slice_cap);
+    const size_t bytes = topk_layout(slice_cap).total;
+    if (bytes > 227 * 1024) return cudaErrorInvalidValue;
+    static int attr_bytes = 0;
+    if ((int)bytes > attr_bytes) {
         cudaError_t e = set_smem_attrs(topk_kernel, (int)bytes);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr_bytes = (int)bytes;
     }
-    if (p.rows <= 0) return cudaSuccess;
-    return launch_pdl(topk_kernel, dim3(p.rows), dim3(kThreads), bytes, stream, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.rows * csize);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = csize;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, topk_kernel, p, csize, slice_cap);
 }
 
 DSA_DEFINE_ERROR_READER(take_error_topk)
