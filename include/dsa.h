@@ -16,7 +16,8 @@
  * Conventions for every entry point:
  *   - Array pointers are DEVICE pointers owned by the caller; libdsa allocates nothing.
  *     Scratch space, where an entry point needs some, is passed in by the caller and
- *     sized by dsa_workspace_bytes().
+ *     sized by dsa_workspace_bytes() (dsa_sparse_mla_decode_noalloc uses a fixed static
+ *     array of the library instead).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
  *     stream).  Argument errors are found on the host and returned before anything is
  *     launched; a failed launch returns DSA_ERR_CUDA.  No exception crosses the ABI.
@@ -30,9 +31,10 @@
  *   - Query rows are grouped by sequence: with T rows per sequence, rows b*T .. b*T+T-1
  *     belong to sequence b.  Row t sits at position q_pos[t] and sees tokens
  *     0 .. q_pos[t] (causal; the query's own token is already cached).
- *   - The library holds no state beyond the device error word and the kernel
- *     attributes it sets once per process; calls on different streams with different
- *     output and workspace buffers may run concurrently.
+ *   - The library holds no state beyond the device error word, the kernel attributes it
+ *     sets once per process and the static scratch of dsa_sparse_mla_decode_noalloc;
+ *     calls on different streams with different output and workspace buffers may run
+ *     concurrently (dsa_sparse_mla_decode_noalloc excepted: see there).
  */
 #ifndef DSA_H
 #define DSA_H
@@ -50,7 +52,9 @@ typedef enum {
     DSA_ERR_UNSUPPORTED = 2, /* a shape this build does not implement */
     DSA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
     DSA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than dsa_workspace_bytes() */
-    DSA_ERR_DEVICE = 5       /* dsa_device_error(): a device-side check fired */
+    DSA_ERR_DEVICE = 5,      /* dsa_device_error(): a device-side check fired */
+    DSA_ERR_SCRATCH_LIMIT = 6 /* dsa_sparse_mla_decode_noalloc: shape needs more scratch
+                                 than DSA_NOALLOC_SCRATCH_BYTES */
 } dsa_status_t;
 
 /*
@@ -127,6 +131,41 @@ dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
                                    int B, int H, int d, int r, int k, float scale,
                                    uint16_t *out, float *lse, void *workspace,
                                    size_t workspace_bytes, void *stream);
+
+/* Size of the fixed device scratch behind dsa_sparse_mla_decode_noalloc (20 MiB). */
+#define DSA_NOALLOC_SCRATCH_BYTES ((size_t)20 << 20)
+
+/*
+ * Sparse MLA decode that allocates nothing and takes no workspace.  The source page has
+ * no counterpart to this entry point: it is a service of the library.  It computes what
+ * dsa_sparse_mla_decode computes, with the same kernels and the same split of the keys,
+ * but keeps the split-KV partial results in a fixed array of DSA_NOALLOC_SCRATCH_BYTES
+ * that libdsa reserves statically on each device, instead of in caller memory.  It is
+ * for callers that cannot allocate device memory on the decode path: a plain C host
+ * program with no device allocator of its own, or a serving loop whose device memory is
+ * all handed out up front, for which a per-call cudaMalloc/cudaFree would also
+ * synchronise the device.
+ *   - Set-up: the first call on each device (that device current) looks the array's
+ *     address up with cudaGetSymbolAddress, which may load libdsa's device code, and
+ *     returns DSA_ERR_CUDA if that fails.  Make this first call before any stream
+ *     capture begins.  Later calls on the device reuse the address and do nothing but
+ *     check the arguments and launch.
+ *   - Limit: a shape for which dsa_workspace_bytes(DSA_OP_SPARSE_MLA, B, 1, H, d, k, 1)
+ *     exceeds DSA_NOALLOC_SCRATCH_BYTES returns DSA_ERR_SCRATCH_LIMIT before anything is
+ *     launched.  The split count keeps rows x splits within the SM count, so on a
+ *     148-SM B300 every supported shape fits (at most 148 x 131,584 bytes).
+ *   - Nothing in the array has to start at zero: each call writes every partial result
+ *     before it reads it.
+ *   - All calls on a device share the array: two calls whose executions overlap (on
+ *     different streams, or from host threads that do not order their streams) race on
+ *     it and their results are undefined.  Calls in order on one stream are safe.
+ * Arguments, layouts and the other errors are those of dsa_sparse_mla_decode.
+ */
+dsa_status_t dsa_sparse_mla_decode_noalloc(const uint16_t *q, const uint16_t *kv_cache,
+                                           const dsa_cache_layout_t *layout,
+                                           const int32_t *idx, int B, int H, int d, int r,
+                                           int k, float scale, uint16_t *out, float *lse,
+                                           void *stream);
 
 /*
  * Sparse MLA prefill: as dsa_sparse_mla_decode with T query rows per sequence, each row

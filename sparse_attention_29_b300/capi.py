@@ -17,13 +17,14 @@ LIB_PATH = os.path.join(HERE, "libdsa.so")
 
 DSA_OK = 0
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_CUDA",
-          4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_DEVICE"}
+          4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_SCRATCH_LIMIT"}
 DSA_OP_INDEXER, DSA_OP_TOPK, DSA_OP_SPARSE_MLA = 0, 1, 2
+DSA_NOALLOC_SCRATCH_BYTES = 20 << 20
 
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
-           "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_shared",
-           "dsa_workspace_bytes", "dsa_device_error")
+           "dsa_sparse_mla_decode", "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_prefill",
+           "dsa_sparse_mla_shared", "dsa_workspace_bytes", "dsa_device_error")
 
 
 class DsaError(RuntimeError):
@@ -63,6 +64,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_topk.argtypes = [P, P, I, I, I, P, P]
     lib.dsa_sparse_mla_decode.restype = I
     lib.dsa_sparse_mla_decode.argtypes = [P, P, LP, P, I, I, I, I, I, F, P, P, P, S, P]
+    lib.dsa_sparse_mla_decode_noalloc.restype = I
+    lib.dsa_sparse_mla_decode_noalloc.argtypes = [P, P, LP, P, I, I, I, I, I, F, P, P, P]
     lib.dsa_sparse_mla_prefill.restype = I
     lib.dsa_sparse_mla_prefill.argtypes = [P, P, LP, P, I, I, I, I, I, I, F, P, P, P, S, P]
     lib.dsa_sparse_mla_shared.restype = I
@@ -131,6 +134,14 @@ def dsa_sparse_mla_decode(q, kv_cache, layout, idx, B, H, d, r, k, scale, out, l
                                       B, H, d, r, k, float(scale), _ptr(out), _ptr(lse),
                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("dsa_sparse_mla_decode", st)
+
+
+def dsa_sparse_mla_decode_noalloc(q, kv_cache, layout, idx, B, H, d, r, k, scale, out, lse,
+                                  stream=None):
+    st = load().dsa_sparse_mla_decode_noalloc(_ptr(q), _ptr(kv_cache), ctypes.byref(layout),
+                                              _ptr(idx), B, H, d, r, k, float(scale),
+                                              _ptr(out), _ptr(lse), _stream(stream))
+    _check("dsa_sparse_mla_decode_noalloc", st)
 
 
 def dsa_sparse_mla_prefill(q, kv_cache, layout, idx, B, T, H, d, r, k, scale, out, lse,

@@ -150,6 +150,35 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
     return from_cuda(launch_sparse_mla(p, maps, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- fixed scratch of dsa_sparse_mla_decode_noalloc ---------------------------------------
+// Callers that cannot allocate device memory on the decode path (a plain C host with no
+// device allocator, a serving loop whose memory is all handed out up front) get the
+// split-KV partials from this array instead of a workspace.  It is part of the module's
+// static storage: nothing here calls cudaMalloc or cudaFree.  The partials need no
+// zeroing (each call writes every partial before the combine reads it); overlapping
+// calls on one device share it and race.
+static __device__ __align__(256) float g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+void *g_noalloc_addr[kMaxDevices];  // per device, set by the first call on that device
+std::mutex g_noalloc_mutex;
+
+// Address of the array on the current device; the first call per device looks it up.
+dsa_status_t noalloc_scratch(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return from_cuda(cudaErrorUnknown);
+    if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return from_cuda(e != cudaSuccess ? e : cudaErrorUnknown);
+        g_noalloc_addr[dev] = p;
+    }
+    *ptr = g_noalloc_addr[dev];
+    return DSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -164,6 +193,7 @@ const char *dsa_status_string(dsa_status_t s) {
         case DSA_ERR_CUDA: return "CUDA error";
         case DSA_ERR_WORKSPACE: return "workspace missing or too small";
         case DSA_ERR_DEVICE: return "device-side check failed";
+        case DSA_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed no-allocation scratch";
     }
     return "unknown status";
 }
@@ -270,6 +300,21 @@ dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
                                    size_t workspace_bytes, void *stream) {
     return mla_common(&q, &kv_cache, 1, layout, idx, B, 1, H, d, r, k, scale, &out,
                       lse ? &lse : nullptr, workspace, workspace_bytes, stream);
+}
+
+dsa_status_t dsa_sparse_mla_decode_noalloc(const uint16_t *q, const uint16_t *kv_cache,
+                                           const dsa_cache_layout_t *layout,
+                                           const int32_t *idx, int B, int H, int d, int r,
+                                           int k, float scale, uint16_t *out, float *lse,
+                                           void *stream) {
+    void *scratch = nullptr;
+    const dsa_status_t st = noalloc_scratch(&scratch);
+    if (st != DSA_OK) return st;
+    const size_t need = dsa_workspace_bytes(DSA_OP_SPARSE_MLA, B, 1, H, d, k, 1);
+    if (need != (size_t)-1 && need > DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_SCRATCH_LIMIT;
+    // invalid shapes (need == -1) are rejected by the shared checks before any use
+    return mla_common(&q, &kv_cache, 1, layout, idx, B, 1, H, d, r, k, scale, &out,
+                      lse ? &lse : nullptr, scratch, DSA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 dsa_status_t dsa_sparse_mla_prefill(const uint16_t *q, const uint16_t *kv_cache,
