@@ -257,6 +257,9 @@ def main():
     ap.add_argument("--sets", type=int, default=3, help="rotating input sets")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="lean run for profiler captures: one input set, no clock pre-roll, "
+                         "no per-kernel loops, graph replay, e2e or CPU baseline")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.warmup < 3:
@@ -280,6 +283,8 @@ def main():
 
     # baseline CPU timing first (before the GPU is busy; host cores only)
     cpu_base = None
+    if args.profile:
+        args.sets, args.no_cpu_baseline, args.no_e2e = 1, True, True
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_base = cpu_baseline(args.workload)
 
@@ -306,7 +311,7 @@ def main():
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         # untimed pre-roll of the same steps, so that the clock samples see this load
-        t_stop, i = time.time() + 1.0, 0
+        t_stop, i = time.time() + (0.0 if args.profile else 1.0), 0
         while time.time() < t_stop:
             step(layers[i % len(layers)])
             i += 1
@@ -369,6 +374,8 @@ def main():
             torch.cuda.synchronize()
         return a.elapsed_time(b) / args.steps
 
+    if args.profile:  # no further launches after the timed steps
+        time_calls = lambda fn: float("nan")  # noqa: E731
     k_idx = time_calls(lambda lay: lay.indexer())
     k_topk = time_calls(lambda lay: lay.topk())
     k_mla = time_calls(lambda lay: lay.mla_shared() if shared else lay.mla())
@@ -376,6 +383,8 @@ def main():
     # ---- the same K steps replayed from a CUDA graph of the C-ABI calls ----------------
     graph_ms = None
     try:
+        if args.profile:
+            raise RuntimeError("skipped in a profile run")
         graphs = []
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
@@ -499,6 +508,8 @@ def main():
         line["e2e"] = e2e
     if cpu_base:
         line["cpu_baseline"] = cpu_base
+    if args.profile:
+        line["note"] = "profile run (lean, for profiler captures): not a measurement"
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

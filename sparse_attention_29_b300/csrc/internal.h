@@ -105,6 +105,8 @@ struct MlaParams {
     float scale_log2;  // softmax scale * log2(e)
     int splits;        // key splits per (row, layer)
     int tiles_per_split;
+    int cluster;       // 1: the splits of a (row, layer) form a thread-block cluster and
+                       // merge their partial results in distributed shared memory
 };
 
 // TMA descriptors of every layer: q viewed as [rows*H, d+r], kv as [num_rows, d+r] (bf16)
@@ -113,6 +115,7 @@ struct MlaMaps {
     CUtensorMap kv[kMaxLayers];
 };
 
+int mla_tile_keys();  // keys per sparse MLA tile (the split unit)
 int mla_num_splits(int rows_times_layers, int k, int num_sms);
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
 cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);

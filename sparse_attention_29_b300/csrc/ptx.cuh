@@ -375,6 +375,42 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef DSA_W8
 
 // ---------------------------------------------------------------------------------
+// thread-block clusters: rank, barrier over every thread of the cluster, and reads of a
+// peer CTA's shared memory (same offset as a local address, in CTA `rank`).  The reads
+// are ordered after the preceding cluster barrier (both are volatile asm) but carry no
+// memory clobber, so that independent reads can be in flight together.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld(const void *local_ptr, uint32_t rank) {
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote));
+    return v;
+}
+
+// Four consecutive 32-bit words (16-byte aligned).
+__device__ __forceinline__ uint4 dsmem_ld4(const void *local_ptr, uint32_t rank) {
+    uint32_t remote;
+    uint4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(remote));
+    return v;
+}
+
+// ---------------------------------------------------------------------------------
 // programmatic dependent launch: a kernel launched with the programmatic-serialization
 // attribute may start while its predecessor in the stream is still running; it must call
 // griddep_wait() before it touches global memory the predecessor may write or read.

@@ -7,31 +7,41 @@
 //     logit[h, j] = scale * q[h, :] . c_j          (key = the whole row)
 //     o[h, :]     = sum_j softmax_j(logit[h, :]) c_j[:d]   (value = the latent part)
 //
-// Mapping onto sm_103a.  The selected rows are gathered 128 at a time with cp.async
-// (16-byte granules, issued by the softmax threads while they would otherwise wait for
-// the next tile; a separate warp resolves row addresses two tiles ahead) into shared
-// memory in the tensor cores' 128-byte-swizzled layout: chunk c of a tile holds dims
-// 64c..64c+63 of the 128 rows.  (TMA gather4 issues at about one instruction per 65
-// cycles per SM, which is ~10 us per 144 KB tile; cp.async from 128 threads is far
-// cheaper to issue.)  That one layout serves both products:
+// Mapping onto sm_103a.  The selected rows are gathered 64 at a time (a tile) with
+// cp.async in 16-byte granules into shared memory in the tensor cores' 128-byte-swizzled
+// layout: chunk c of a tile holds dims 64c..64c+63 of its 64 rows.  That one layout
+// serves both products:
 //   S^T[key, head]  = C[key, :] . Q[head, :]      A = C (K-major), B = Q (K-major)
 //   O^T[dim, head] += C[key, dim]^T P^T[key, head] A = C^T (MN-major), B = P^T (MN-major)
-// so both run as M = 128 tcgen05 MMAs (keys resp. latent dims on M, the 64 heads on N)
-// with fp32 accumulators in tensor memory (S: 64 columns, O: 4 x 64 columns).  After
-// tcgen05.ld a softmax thread owns one key's 64 head logits; per-head maxima are
-// reduced across the 128 keys of the tile with a transposing warp butterfly.  The
-// probabilities are written (bf16) over the tile's rope chunk, which S no longer needs.
-// One thread issues ~60-80 cycles per tcgen05.mma and a tile needs 68 of them (36 for S,
-// 32 for O), so two issuer warps split the work: each accumulates half of the S chunks
-// into its own S^T copy (the softmax adds the two) and runs half of the O M-blocks.
-// Online softmax rescales O in tensor memory only when a head's running maximum grows
-// by more than 2^8 (the result is the same; the unnormalised terms just stay < 2^8).
-// The query (64 heads x 576 x 2 B = 72 KB) and one tile (144 KB) fill shared memory,
-// so the next tile's gather is overlapped at chunk granularity: chunks are refilled as
-// soon as the O product that reads them has completed.
+// S^T runs as M = 64 tcgen05 MMAs (keys on M), O^T as M = 128 MMAs (latent dims on M),
+// both with the 64 heads on N and fp32 accumulators in tensor memory.
 //
-// Rows with few keys are split over several CTAs (split-KV); each writes unnormalised
-// partial results that a combine kernel merges with the log-sum-exp rule.
+// The query (64 heads x 576 x 2 B = 72 KB) and two tiles (2 x 72 KB) fill shared memory,
+// so tile i+1 is gathered while tile i is in the products and the softmax.  The gather
+// is the pacing item: one SM moves about 35-40 GB/s of 16-byte cp.async only when many
+// warps issue them from precomputed row addresses, so eight warps do nothing else
+// (row addresses for the next tile are resolved while the current one is in flight).
+// Three more warps issue the MMAs, one thread each (a thread issues a tcgen05.mma about
+// every 55 cycles): two split the S chunks, each into its own accumulator (the softmax
+// adds the two), and one runs the O product, so that O of tile i never waits behind S
+// of tile i+1.  S^T is double-buffered in tensor memory, so S of tile i+1 overlaps the
+// softmax of tile i.
+//
+// Softmax: the M = 64 accumulator puts key 16w + i in TMEM lane 32w + i (w = warp,
+// i < 16); a 16x32bx2 tcgen05.ld hands thread i < 16 of warp w heads 0-31 of that key
+// and thread 16 + i heads 32-63, so all 128 softmax threads work.  Per-head maxima are
+// reduced over the tile's 64 keys with a transposing butterfly over 16 lanes, then
+// across the four warps.  The probabilities are written (bf16) over the tile's rope
+// chunk, which S no longer needs.  Online softmax rescales O in tensor memory only when
+// a head's running maximum grows by more than 2^8 (the result is the same; the
+// unnormalised terms just stay < 2^8).
+//
+// Rows with few keys are split over several CTAs (split-KV), merged with the log-sum-exp
+// rule.  Up to kMaxClusterSplits splits of a row run as one thread-block cluster: each CTA
+// leaves its unnormalised O, running maxima and sums in its shared memory and every CTA
+// then finishes a slice of the latent dims from all of them through distributed shared
+// memory (no global round trip, no second kernel).  More splits than that write partial
+// results to the caller's workspace for a combine kernel.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -40,19 +50,26 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 224;      // warps 0-3 softmax + gather + epilogue, 4 and 6 MMA, 5 rows
-constexpr int kSoftmaxThreads = 128;
-constexpr int kMmaWarp = 4;        // MMA issuer 0 (also owns the tensor memory)
-constexpr int kMmaWarp2 = 6;       // MMA issuer 1
-constexpr int kProducerWarp = 5;
-constexpr int kTileKeys = 128;
-constexpr int kHeads = 64;         // heads padded to 64 (N of both products)
-constexpr int kChunkBytes = kTileKeys * 128;  // 64 dims x 128 keys x 2 B
+constexpr int kThreads = 512;       // 16 warps, roles below
+constexpr int kSoftmaxThreads = 128;  // warps 0-3: softmax + epilogue
+constexpr int kGatherWarp0 = 4;       // warps 4-11: gathers
+constexpr int kGatherThreads = 256;
+constexpr int kMmaWarp = 12;          // S issuer 0 (also owns the tensor memory)
+constexpr int kMmaWarp2 = 13;         // S issuer 1
+constexpr int kQWarp = 14;            // query TMA
+constexpr int kOWarp = 15;            // O issuer
+constexpr int kTileKeys = 64;
+constexpr int kHeads = 64;            // heads padded to 64 (N of both products)
+constexpr int kChunkBytes = kTileKeys * 128;  // 64 dims x 64 keys x 2 B
 constexpr int kQChunkBytes = kHeads * 128;    // 64 dims x 64 heads x 2 B
 constexpr float kRescaleLog2 = 8.f;           // lazy rescale threshold (log2 units)
+constexpr int kMaxClusterSplits = 8;          // portable cluster size
+
+// named barriers: 1 softmax sync, 2 softmax OR, 3 gather sync, 4 gather OR
+constexpr int kBarSm = 1, kBarSmOr = 2, kBarGa = 3, kBarGaOr = 4;
 
 struct MlaSmem {
-    uint32_t q, tile, rows, red, rn, alpha, lsum, bars, total;
+    uint32_t q, tile, ptrs, red, rn, alpha, lsum, wts, bars, total;
 };
 
 __host__ __device__ inline MlaSmem mla_smem(int nch) {
@@ -60,10 +77,10 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     uint32_t off = 0;
     s.q = off;
     off += (uint32_t)nch * kQChunkBytes;
-    s.tile = off;
-    off += (uint32_t)nch * kChunkBytes;
-    s.rows = off;
-    off += 2 * kTileKeys * 4;
+    s.tile = off;  // two tile buffers
+    off += 2u * (uint32_t)nch * kChunkBytes;
+    s.ptrs = off;  // [2][64] row addresses
+    off += 2 * kTileKeys * 8;
     s.red = off;
     off += 4 * kHeads * 4;
     s.rn = off;
@@ -72,8 +89,10 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     off += kHeads * 4;
     s.lsum = off;
     off += kHeads * 4;
+    s.wts = off;  // cluster merge: [split][head] weights
+    off += kMaxClusterSplits * kHeads * 4;
     s.bars = off;
-    off += 20 * 8 + 16;
+    off += 16 * 8 + 16;
     s.total = off;
     return s;
 }
@@ -99,9 +118,8 @@ __device__ __forceinline__ int64_t resolve_row(const CacheLayout &L, int b, int 
     return (row >= 0 && row < L.num_rows) ? row : -1;
 }
 
-// Transposing butterfly over the 32 lanes of a warp: on entry x[0..63] are one key's
-// values for heads 0..63; on exit x[0], x[1] hold heads 2*lane, 2*lane+1 combined over
-// all 32 keys of the warp (max if kMax, else sum).
+// Transposing butterfly over 32 lanes: on entry x[0..63] are one key's values for heads
+// 0..63; on exit x[0], x[1] hold heads 2*lane, 2*lane+1 combined over the warp's keys.
 template <bool kMax>
 __device__ __forceinline__ void warp_transpose_reduce(float (&x)[64], int lane) {
 #pragma unroll
@@ -119,27 +137,49 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&x)[64], int lane) 
     }
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
-    uint32_t (&r)[64] = reinterpret_cast<uint32_t (&)[64]>(x);
-    tmem_ld32(taddr, reinterpret_cast<uint32_t (&)[32]>(r[0]));
-    tmem_ld32(taddr + 32, reinterpret_cast<uint32_t (&)[32]>(r[32]));
-    tmem_ld_wait();
+// The same over the 16 lanes of each half-warp with 32 values (heads of one half): on
+// exit x[0], x[1] hold heads 2*(lane & 15), +1 of the half, combined over its 16 keys.
+template <bool kMax>
+__device__ __forceinline__ void half_transpose_reduce(float (&x)[32], int lane) {
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        const int half = 16 >> step;
+        const int off = 8 >> step;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? x[i] : x[i + half];
+            const float keep = upper ? x[i + half] : x[i];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+            x[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
 }
 
-// S^T row of this thread's key: the sum of the two issuers' parts (columns 0-63, 64-127).
-__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, float (&x)[64]) {
-    uint32_t (&r)[64] = reinterpret_cast<uint32_t (&)[64]>(x);
-    tmem_ld32(taddr, reinterpret_cast<uint32_t (&)[32]>(r[0]));
-    tmem_ld32(taddr + 32, reinterpret_cast<uint32_t (&)[32]>(r[32]));
-    uint32_t y[32];
-    tmem_ld32(taddr + 64, y);
+// 16x32bx2 load of 32 columns: thread i < 16 of the warp reads TMEM lane (base + i),
+// columns [col, col + 32); thread 16 + i reads lane (base + i), columns [col + 32, col + 64).
+__device__ __forceinline__ void tmem_ld_pair32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+// This thread's key, 32 heads of S^T: the sum of the two issuers' parts (64 columns apart).
+__device__ __forceinline__ void tmem_ld_s(uint32_t taddr, float (&x)[32]) {
+    uint32_t c[32];
+    tmem_ld_pair32(taddr, reinterpret_cast<uint32_t (&)[32]>(x));
+    tmem_ld_pair32(taddr + 64, c);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] += __uint_as_float(y[i]);
-    tmem_ld32(taddr + 96, y);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[32 + i] += __uint_as_float(y[i]);
+    for (int i = 0; i < 32; ++i) x[i] += __uint_as_float(c[i]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -147,32 +187,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nv = p.d / 64;             // latent (value) chunks
     const int nch = nv + 1;              // + the rope chunk
     const int nmb = (nv + 1) / 2;        // M-blocks of the O product (128 dims each)
-    const int ngroups = nmb + 1;         // gather groups: V chunk pairs, then rope
     const int rope = nv;                 // index of the rope chunk (later: P)
+    const int G = nch * 8;               // 16-byte granules per gathered row
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const MlaSmem L = mla_smem(nch);
     uint8_t *qs = smem + L.q;
-    uint8_t *tile = smem + L.tile;
-    uint8_t *pslot = tile + rope * kChunkBytes;
-    int32_t *rows_sm = (int32_t *)(smem + L.rows);   // [2][128] physical rows, -1 invalid
+    uint8_t *tiles = smem + L.tile;
+    const uint8_t **ptrs = (const uint8_t **)(smem + L.ptrs);  // [2][64], null: invalid
     float *red = (float *)(smem + L.red);
     float *rn = (float *)(smem + L.rn);
     float *alpha = (float *)(smem + L.alpha);
     float *lsum = (float *)(smem + L.lsum);
     uint64_t *bars = (uint64_t *)(smem + L.bars);
-    uint64_t *full = bars;           // [ngroups] chunk groups landed
-    uint64_t *freeb = bars + 5;      // [ngroups] chunk groups free again
-    uint64_t *s_full = bars + 10;    // S^T of the tile is in TMEM
-    uint64_t *p_ready = bars + 11;   // P^T written (and O rescaled)
-    uint64_t *o_done = bars + 12;    // O^T product of the tile complete
-    uint64_t *drain = bars + 13;
-    uint64_t *q_full = bars + 14;
-    uint64_t *addr_ready = bars + 15;  // [2] row table of a tile written
-    uint64_t *addr_empty = bars + 17;  // [2] row table of a tile no longer needed
-    volatile int *abort_flag = (volatile int *)(bars + 20);
-    uint32_t *tmem_base_sm = (uint32_t *)(bars + 20) + 1;
+    uint64_t *full = bars;           // [2] tile buffer landed
+    uint64_t *tfree = bars + 2;      // [2] tile buffer read by both products
+    uint64_t *s_full = bars + 4;     // [2] S^T buffer written
+    uint64_t *s_free = bars + 6;     // [2] S^T buffer read by the softmax
+    uint64_t *p_ready = bars + 8;    // [2] P of the tile in its buffer (and O rescaled)
+    uint64_t *o_done = bars + 10;    // O^T product of a tile complete
+    uint64_t *q_full = bars + 11;
+    uint64_t *drain = bars + 12;
+    volatile int *abort_flag = (volatile int *)(bars + 16);
+    uint32_t *tmem_base_sm = (uint32_t *)(bars + 16) + 1;
+    const size_t buf_bytes = (size_t)nch * kChunkBytes;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -197,32 +236,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         rn[tid] = -INFINITY;
         alpha[tid] = 1.f;
     }
-    if (p.r < 64) {
-        // columns past d + r of the rope chunk: keep them zero in case the copy leaves
-        // out-of-range columns untouched
-        for (int e = tid; e < kTileKeys * 8; e += kThreads)
-            *(uint4 *)(tile + rope * kChunkBytes + e * 16) = make_uint4(0, 0, 0, 0);
-        fence_proxy_async();
-    }
     if (tid == 0) {
-        for (int g = 0; g < ngroups; ++g) {
-            mbar_init(&full[g], kSoftmaxThreads);
-            mbar_init(&freeb[g], g == ngroups - 1 ? 2 : 1);  // rope/P chunk: both issuers
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full[i], kGatherThreads);
+            mbar_init(&tfree[i], 1);
+            mbar_init(&s_full[i], 2);
+            mbar_init(&s_free[i], kSoftmaxThreads);
+            mbar_init(&p_ready[i], kSoftmaxThreads);
         }
-        mbar_init(s_full, 2);
-        mbar_init(p_ready, kSoftmaxThreads);
-        mbar_init(o_done, 2);
-        mbar_init(drain, 2);
+        mbar_init(o_done, 1);
         mbar_init(q_full, 1);
-        mbar_init(&addr_ready[0], 32);
-        mbar_init(&addr_ready[1], 32);
-        mbar_init(&addr_empty[0], kSoftmaxThreads);
-        mbar_init(&addr_empty[1], kSoftmaxThreads);
+        mbar_init(drain, 3);
         *abort_flag = 0;
         fence_barrier_init();
     }
     uint32_t tmem_cols = 32;
-    while (tmem_cols < (uint32_t)(2 * kHeads + nmb * kHeads)) tmem_cols <<= 1;
+    while (tmem_cols < (uint32_t)(4 * kHeads + nmb * kHeads)) tmem_cols <<= 1;
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_base_sm, tmem_cols);
         tmem_relinquish();
@@ -231,67 +260,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_sm;
-    const uint32_t tS = tmem;          // 2 x 64 columns: one S^T part per MMA issuer
-    const uint32_t tO = tmem + 128;    // nmb x 64 columns
+    const uint32_t tS = tmem;          // [2 buffers][2 issuer parts] x 64 columns
+    const uint32_t tO = tmem + 256;    // nmb x 64 columns
 
-    if (warp == kProducerWarp) {
-        // ===== query TMA, then the physical row of every selected key, 2 tiles ahead =====
-        if (lane == 0) {
+    // Roles by warpgroup, each with its register share: the softmax warpgroup holds a
+    // key's logits, probabilities and running sums; the others need few.  512 threads
+    // launch with 128 registers each (65536); after the adjustment 128 x 232 +
+    // 384 x 80 = 60416 are in use.
+    if (warp >= kMmaWarp) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+      if (warp == kQWarp) {
+        // ================= query TMA =================
+        if (lane == 0 && ntiles > 0) {
             const CUtensorMap *qmap = &maps.q[layer];
             prefetch_tmap(qmap);
             mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
             for (int c = 0; c < nch; ++c)
                 tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
         }
-        for (int li = 0; li < ntiles; ++li) {
-            const int buf = li & 1;
-            if (li >= 2) {
-                const bool got = mbar_wait(&addr_empty[buf], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
-                if (!__all_sync(0xffffffffu, got)) break;
-            }
-            const int j0 = (t_begin + li) * kTileKeys + lane * 4;
-            int y[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = j0 + e;
-                int64_t r = -1;
-                if (j < p.k) {
-                    const int s = __ldg(idx_row + j);
-                    if (s >= 0) {
-                        r = resolve_row(p.layout, b, s);
-                        if (r < 0) record_error(KID_MLA, ERR_BAD_INDEX);
-                    }
-                }
-                y[e] = (int)r;
-            }
-            *(int4 *)(rows_sm + buf * kTileKeys + lane * 4) = make_int4(y[0], y[1], y[2], y[3]);
-            mbar_arrive(&addr_ready[buf]);
-        }
-    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
-        // ================= MMA issuers =================
-        // issuer r: S chunks [c_lo, c_hi) into its own S^T copy, O M-blocks [m_lo, m_hi)
+      } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ================= S issuers =================
+        // issuer r: S chunks [c_lo, c_hi) into its own S^T part
         const int r = warp == kMmaWarp ? 0 : 1;
-        const int nch_a = (nch + 1) / 2, nmb_a = (nmb + 1) / 2;
+        const int nch_a = (nch + 1) / 2;
         const int c_lo = r == 0 ? 0 : nch_a, c_hi = r == 0 ? nch_a : nch;
-        const int m_lo = r == 0 ? 0 : nmb_a, m_hi = r == 0 ? nmb_a : nmb;
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16(128, kHeads, false, false);
-            const uint32_t idO = idesc_bf16(128, kHeads, true, true);
-            const uint32_t tile_a = smem_u32(tile), q_a = smem_u32(qs), p_a = smem_u32(pslot);
-            const uint32_t tSr = tS + (uint32_t)(r * kHeads);
+            const uint32_t idS = idesc_bf16(64, kHeads, false, false);
+            const uint32_t tiles_a = smem_u32(tiles), q_a = smem_u32(qs);
             bool ok = ntiles == 0 || mbar_wait(q_full, 0, KID_MLA, abort_flag);
             for (int li = 0; li < ntiles && ok; ++li) {
-                // S^T part = C . Q^T over this issuer's chunks, as their gather groups land
-                int waited = -1;
-                for (int c = c_lo; c < c_hi && ok; ++c) {
-                    const int g = c == rope ? ngroups - 1 : c / 2;
-                    if (g != waited) {
-                        ok = mbar_wait(&full[g], li & 1, KID_MLA, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
-                        waited = g;
-                    }
+                const int bi = li & 1;
+                ok = mbar_wait(&full[bi], (li >> 1) & 1, KID_MLA, abort_flag);
+                if (ok && li >= 2) ok = mbar_wait(&s_free[bi], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
+                const uint32_t tile_a = tiles_a + (uint32_t)(bi * buf_bytes);
+                const uint32_t tSr = tS + (uint32_t)(bi * 2 * kHeads + r * kHeads);
+                for (int c = c_lo; c < c_hi; ++c) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
@@ -299,21 +305,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tSr, ad, bd, idS, (c > c_lo || kk > 0) ? 1u : 0u);
                     }
                 }
-                if (!ok) break;
-                mma_commit(s_full);
-                // O^T += C^T . P^T once the probabilities are in place
-                if (!mbar_wait(p_ready, li & 1, KID_MLA, abort_flag)) break;
+                mma_commit(&s_full[bi]);
+            }
+            mma_commit(drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+      } else if (warp == kOWarp) {
+        // ================= O issuer: O^T += C^T . P^T once a tile's P is in place ====
+        if (lane == 0) {
+            const uint32_t idO = idesc_bf16(128, kHeads, true, true);
+            const uint32_t tiles_a = smem_u32(tiles);
+            for (int li = 0; li < ntiles; ++li) {
+                const int bi = li & 1;
+                if (!mbar_wait(&p_ready[bi], (li >> 1) & 1, KID_MLA, abort_flag)) break;
                 tc_fence_after();
-                for (int j = m_lo; j < m_hi; ++j) {
+                const uint32_t tile_a = tiles_a + (uint32_t)(bi * buf_bytes);
+                const uint32_t p_a = tile_a + rope * kChunkBytes;
+                for (int j = 0; j < nmb; ++j) {
 #pragma unroll
                     for (int ks = 0; ks < kTileKeys / 16; ++ks) {
                         const uint64_t ad = make_sdesc(tile_a + 2 * j * kChunkBytes + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
                         const uint64_t bd = make_sdesc(p_a + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
                         mma_bf16(tO + j * kHeads, ad, bd, idO, (li > 0 || ks > 0) ? 1u : 0u);
                     }
-                    if (j < ngroups - 1) mma_commit(&freeb[j]);
                 }
-                mma_commit(&freeb[ngroups - 1]);
+                mma_commit(&tfree[bi]);
                 mma_commit(o_done);
             }
             mma_commit(drain);
@@ -322,111 +341,137 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else {
-        // ================= softmax + epilogue (128 threads, one key each) ===============
-        const int kl = warp * 32 + lane;          // key lane == TMEM lane
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        float lp[64];
-#pragma unroll
-        for (int h = 0; h < 64; ++h) lp[h] = 0.f;
-        const uint16_t *kv = p.kv[layer];
-        const int D = p.d + p.r;
-        // Gather group g of tile li (its row table must be ready and the group free):
-        // thread t owns one 16-byte column of the group and every 8th (or 16th) row, so
-        // its swizzled destination advances by a constant 1 KB (or 2 KB) per step.
-        auto gather_group = [&](int li, int g) {
-            const int32_t *rows = rows_sm + (li & 1) * kTileKeys;
-            const bool is_rope = (g == ngroups - 1);
-            const int c0 = is_rope ? rope : 2 * g;
-            const int nck = is_rope ? 1 : min(2, nv - 2 * g);
-            if (nck == 2) {
-                const int gc = kl & 15, rb = kl >> 4;
-                const int c = c0 + (gc >> 3), gr = gc & 7;
-                uint8_t *dst = tile + c * kChunkBytes + rb * 128 + ((gr ^ rb) << 4);
-                const int col = c * 64 + gr * 8;
-#pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    const int r = rows[rb + 8 * i];
-                    cp_async_16(dst + i * 1024, r >= 0 ? kv + (int64_t)r * D + col : kv, r >= 0 ? 16u : 0u);
-                }
-            } else {
-                const int gr = kl & 7, rb = kl >> 3;  // rows rb + 16 i
-                uint8_t *dst = tile + c0 * kChunkBytes + (rb >> 3) * 1024 + (rb & 7) * 128 + ((gr ^ (rb & 7)) << 4);
-                int col = c0 * 64 + gr * 8;
-                bool in = true;
-                if (is_rope) {
-                    col = p.d + gr * 8;
-                    in = gr * 8 < p.r;
-                }
-#pragma unroll 4
-                for (int i = 0; i < 8; ++i) {
-                    const int r = rows[rb + 16 * i];
-                    const bool go = in && r >= 0;
-                    cp_async_16(dst + i * 2048, go ? kv + (int64_t)r * D + col : kv, go ? 16u : 0u);
+      }
+    } else if (warp >= kGatherWarp0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+        // ================= gathers =================
+        const int gt = tid - kGatherWarp0 * 32;
+        const uint8_t *kv_bytes = reinterpret_cast<const uint8_t *>(p.kv[layer]);
+        const int64_t row_bytes = (int64_t)(p.d + p.r) * 2;
+        auto resolve = [&](int li, int key) -> const uint8_t * {
+            const int j = (t_begin + li) * kTileKeys + key;
+            if (j >= p.k) return nullptr;
+            const int s = __ldg(idx_row + j);
+            if (s < 0) return nullptr;
+            const int64_t r = resolve_row(p.layout, b, s);
+            if (r < 0) {
+                record_error(KID_MLA, ERR_BAD_INDEX);
+                return nullptr;
+            }
+            return kv_bytes + r * row_bytes;
+        };
+        if (gt < kTileKeys && ntiles > 0) ptrs[gt] = resolve(0, gt);
+        named_bar_sync(kBarGa, kGatherThreads);
+        // thread gt copies granules q = gt, gt + 256, ... of the tile (q = row * G + gran)
+        const int nq = kTileKeys * G;
+        const int r_start = gt / G, g_start = gt - r_start * G;
+        const int dr = kGatherThreads / G, dg = kGatherThreads - dr * G;
+        for (int li = 0; li < ntiles; ++li) {
+            const int bi = li & 1;
+            if (li >= 2) {
+                const bool got = mbar_wait(&tfree[bi], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
+                if (named_bar_or(kBarGaOr, kGatherThreads, !got)) break;
+            }
+            uint8_t *buf = tiles + bi * buf_bytes;
+            const uint8_t *const *pt = ptrs + bi * kTileKeys;
+            int r = r_start, g = g_start;
+#pragma unroll 6
+            for (int q = gt; q < nq; q += kGatherThreads) {
+                const int c = g >> 3, gi = g & 7;
+                const uint8_t *base = pt[r];
+                const bool ok = base != nullptr && (c < nv || gi * 8 < p.r);
+                cp_async_16(buf + c * kChunkBytes + r * 128 + ((gi ^ (r & 7)) << 4),
+                            ok ? base + g * 16 : kv_bytes, ok ? 16u : 0u);
+                g += dg;
+                r += dr;
+                if (g >= G) {
+                    g -= G;
+                    ++r;
                 }
             }
-            cp_async_arrive(&full[g]);
+            cp_async_arrive(&full[bi]);
+            if (gt < kTileKeys && li + 1 < ntiles) ptrs[(bi ^ 1) * kTileKeys + gt] = resolve(li + 1, gt);
+            named_bar_sync(kBarGa, kGatherThreads);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
+        // ================= softmax + epilogue (128 threads) ===============
+        // thread: key 16*warp + (lane & 15) of the tile, heads hh*32 .. hh*32+31
+        const int key = warp * 16 + (lane & 15);
+        const int hh = lane >> 4;
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        float lp[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) lp[h] = 0.f;
+        // validity of this thread's key in tile li (same rule as the gathers)
+        auto key_valid = [&](int li) -> bool {
+            const int j = (t_begin + li) * kTileKeys + key;
+            if (li >= ntiles || j >= p.k) return false;
+            const int s = __ldg(idx_row + j);
+            return s >= 0 && resolve_row(p.layout, b, s) >= 0;
         };
         bool ok = true;
-        // tile 0: every group is free
-        if (ntiles > 0) {
-            const bool got = mbar_wait(&addr_ready[0], 0, KID_MLA, abort_flag);
-            if (named_bar_or(2, kSoftmaxThreads, !got)) ok = false;
-            else
-                for (int g = 0; g < ngroups; ++g) gather_group(0, g);
-        }
+        bool valid_next = key_valid(0);
         for (int li = 0; li < ntiles && ok; ++li) {
+            const int bi = li & 1;
+            const bool valid = valid_next;
+            valid_next = key_valid(li + 1);
             // every decision that guards a named barrier or a warp-collective TMEM access
             // is made uniform over the 128 threads first
-            const bool got = mbar_wait(s_full, li & 1, KID_MLA, abort_flag);
-            if (named_bar_or(2, kSoftmaxThreads, !got)) { ok = false; break; }
+            const bool got = mbar_wait(&s_full[bi], (li >> 1) & 1, KID_MLA, abort_flag);
+            if (named_bar_or(kBarSmOr, kSoftmaxThreads, !got)) { ok = false; break; }
             tc_fence_after();
-            const bool valid = rows_sm[(li & 1) * kTileKeys + kl] >= 0;
-            float x[64];
-            tmem_ld_s(tS + lane_addr, x);
+            const uint32_t taS = tS + lane_addr + (uint32_t)(bi * 2 * kHeads);
+            float x[32];
+            tmem_ld_s(taS, x);
 #pragma unroll
-            for (int h = 0; h < 64; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-            warp_transpose_reduce<true>(x, lane);
-            red[warp * 64 + 2 * lane] = x[0];
-            red[warp * 64 + 2 * lane + 1] = x[1];
-            named_bar_sync(1, kSoftmaxThreads);
+            for (int h = 0; h < 32; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+            half_transpose_reduce<true>(x, lane);
+            red[warp * 64 + hh * 32 + 2 * (lane & 15)] = x[0];
+            red[warp * 64 + hh * 32 + 2 * (lane & 15) + 1] = x[1];
+            named_bar_sync(kBarSm, kSoftmaxThreads);
             bool need = false;
-            if (kl < kHeads) {
-                const float m = fmaxf(fmaxf(red[kl], red[64 + kl]), fmaxf(red[128 + kl], red[192 + kl]));
-                const float rold = rn[kl];
+            if (tid < kHeads) {
+                const float m = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+                const float rold = rn[tid];
                 need = m > rold + kRescaleLog2;
                 const float rnew = need ? m : rold;
-                alpha[kl] = need ? ex2_approx(rold - rnew) : 1.f;
-                rn[kl] = rnew;
+                alpha[tid] = need ? ex2_approx(rold - rnew) : 1.f;
+                rn[tid] = rnew;
             }
-            const bool any = named_bar_or(2, kSoftmaxThreads, need);
-            // probabilities of this key for every head
-            tmem_ld_s(tS + lane_addr, x);
-            uint32_t pk[32];
+            const bool any = named_bar_or(kBarSmOr, kSoftmaxThreads, need);
+            // probabilities of this key for its 32 heads (S^T is read a second time)
+            tmem_ld_s(taS, x);
+            tc_fence_before();
+            mbar_arrive(&s_free[bi]);
+            uint32_t pk[16];
 #pragma unroll
-            for (int h = 0; h < 64; h += 2) {
+            for (int i = 0; i < 32; i += 2) {
                 float pr[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const float rr = rn[h + e];
-                    const float lg = x[h + e] * p.scale_log2;
+                    const float rr = rn[hh * 32 + i + e];
+                    const float lg = x[i + e] * p.scale_log2;
                     pr[e] = (valid && rr != -INFINITY) ? ex2_approx(lg - rr) : 0.f;
                 }
                 const __nv_bfloat162 pb = __floats2bfloat162_rn(pr[0], pr[1]);
                 const float2 pf = __bfloat1622float2(pb);
-                lp[h] = fmaf(lp[h], alpha[h], pf.x);
-                lp[h + 1] = fmaf(lp[h + 1], alpha[h + 1], pf.y);
-                pk[h >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
+                lp[i] = fmaf(lp[i], alpha[hh * 32 + i], pf.x);
+                lp[i + 1] = fmaf(lp[i + 1], alpha[hh * 32 + i + 1], pf.y);
+                pk[i >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
             }
+            uint8_t *pslot = tiles + bi * buf_bytes + rope * kChunkBytes;
 #pragma unroll
-            for (int gr = 0; gr < 8; ++gr)
-                *(uint4 *)(pslot + swz128(kl, gr)) =
-                    make_uint4(pk[gr * 4 + 0], pk[gr * 4 + 1], pk[gr * 4 + 2], pk[gr * 4 + 3]);
+            for (int q = 0; q < 4; ++q)
+                *(uint4 *)(pslot + swz128(key, hh * 4 + q)) =
+                    make_uint4(pk[q * 4 + 0], pk[q * 4 + 1], pk[q * 4 + 2], pk[q * 4 + 3]);
             fence_proxy_async();
             if (any && li > 0) {
-                // rescale the running O (needs the previous tile's O product complete)
+                // rescale the running O (needs the previous tile's O product complete);
+                // here thread = TMEM lane = latent dim within each M-block
                 const bool got_o = mbar_wait(o_done, (li - 1) & 1, KID_MLA, abort_flag);
-                if (named_bar_or(2, kSoftmaxThreads, !got_o)) {
+                if (named_bar_or(kBarSmOr, kSoftmaxThreads, !got_o)) {
                     ok = false;
                 } else {
                     tc_fence_after();
@@ -447,38 +492,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(p_ready);
-            if (!ok) break;
-            mbar_arrive(&addr_empty[li & 1]);  // row table of tile li fully used
-            // gathers of the next tile, group by group as the O product frees them
-            if (li + 1 < ntiles) {
-                bool g_ok = mbar_wait(&addr_ready[(li + 1) & 1], ((li + 1) >> 1) & 1, KID_MLA, abort_flag);
-                if (named_bar_or(2, kSoftmaxThreads, !g_ok)) { ok = false; break; }
-                for (int g = 0; g < ngroups; ++g) {
-                    g_ok = mbar_wait(&freeb[g], li & 1, KID_MLA, abort_flag);
-                    if (named_bar_or(2, kSoftmaxThreads, !g_ok)) { ok = false; break; }
-                    gather_group(li + 1, g);
-                }
-                if (!ok) break;
-            }
+            mbar_arrive(&p_ready[bi]);
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
         // ---- epilogue ----
-        named_bar_sync(1, kSoftmaxThreads);
+        named_bar_sync(kBarSm, kSoftmaxThreads);
         if (ntiles > 0) {
             const bool got = ok && mbar_wait(o_done, (ntiles - 1) & 1, KID_MLA, abort_flag);
-            ok = !named_bar_or(2, kSoftmaxThreads, !got);
+            ok = !named_bar_or(kBarSmOr, kSoftmaxThreads, !got);
         }
         tc_fence_after();
-        warp_transpose_reduce<false>(lp, lane);
-        red[warp * 64 + 2 * lane] = lp[0];
-        red[warp * 64 + 2 * lane + 1] = lp[1];
-        named_bar_sync(1, kSoftmaxThreads);
-        if (kl < kHeads) lsum[kl] = red[kl] + red[64 + kl] + red[128 + kl] + red[192 + kl];
-        named_bar_sync(1, kSoftmaxThreads);
+        half_transpose_reduce<false>(lp, lane);
+        red[warp * 64 + hh * 32 + 2 * (lane & 15)] = lp[0];
+        red[warp * 64 + hh * 32 + 2 * (lane & 15) + 1] = lp[1];
+        named_bar_sync(kBarSm, kSoftmaxThreads);
+        if (tid < kHeads) lsum[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+        named_bar_sync(kBarSm, kSoftmaxThreads);
+        const int kl = tid;  // TMEM lane = latent dim within an M-block
         const int unit_out = row * p.layers + layer;
         const bool have_o = ok && ntiles > 0;
-        if (p.splits == 1) {
+        if (p.cluster) {
+            // unnormalised O into this CTA's (now idle) tile buffers as [64 heads][d] fp32
+            // (consecutive threads: consecutive dims); rn and lsum stay put.  The cluster
+            // merges them after the next cluster barrier.
+            float *part = reinterpret_cast<float *>(tiles);
+            for (int mb = 0; mb < nmb; ++mb) {
+                const int dim = mb * 128 + kl;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    if (have_o) {
+                        tmem_ld32(tO + lane_addr + mb * kHeads + half * 32, v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    }
+                    if (dim < p.d) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) part[(half * 32 + e) * p.d + dim] = __uint_as_float(v[e]);
+                    }
+                }
+            }
+        } else if (p.splits == 1) {
             uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
             for (int mb = 0; mb < nmb; ++mb) {
                 const int dim = mb * 128 + kl;
@@ -539,6 +594,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (p.cluster) {
+        // ===== merge the cluster's splits: CTA `split` finishes dims [d_lo, d_hi) =====
+        cluster_sync();  // every CTA's O, maxima (rn) and sums (lsum) are in place
+        float *wts = (float *)(smem + L.wts);
+        if (tid < kHeads) {
+            // every split's maximum and sum for head h, all loads in flight at once
+            const int h = tid;
+            float rs[kMaxClusterSplits], ls[kMaxClusterSplits];
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                rs[s] = s < p.splits ? __uint_as_float(dsmem_ld(&rn[h], (uint32_t)s)) : -INFINITY;
+                ls[s] = s < p.splits ? __uint_as_float(dsmem_ld(&lsum[h], (uint32_t)s)) : 0.f;
+            }
+            float R = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) R = fmaxf(R, rs[s]);
+            float Lsum = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                rs[s] = (R == -INFINITY || rs[s] == -INFINITY) ? 0.f : ex2_approx(rs[s] - R);
+                Lsum = fmaf(rs[s], ls[s], Lsum);
+            }
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) wts[s * kHeads + h] = rs[s] * inv;
+            if (split == 0 && h < p.H && p.lse[layer])
+                p.lse[layer][(int64_t)row * p.H + h] =
+                    Lsum > 0.f ? (R + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        }
+        __syncthreads();
+        const int ds = ((p.d + p.splits - 1) / p.splits + 3) & ~3;
+        const int d_lo = min(p.d, split * ds), d_hi = min(p.d, d_lo + ds);
+        const int ng = (d_hi - d_lo) >> 2;  // groups of 4 dims
+        const float *part = reinterpret_cast<const float *>(tiles);
+        uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
+        for (int it = tid; it < ng * kHeads; it += kThreads) {
+            const int h = it / ng, dim = d_lo + 4 * (it - h * ng);  // consecutive threads: dims
+            const float *src = part + h * p.d + dim;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int s0 = 0; s0 < kMaxClusterSplits; s0 += 4) {
+                if (s0 >= p.splits) break;
+                uint4 v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[e] = s0 + e < p.splits ? dsmem_ld4(src, (uint32_t)(s0 + e)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float w = wts[(s0 + e) * kHeads + h];
+                    acc.x = fmaf(w, __uint_as_float(v[e].x), acc.x);
+                    acc.y = fmaf(w, __uint_as_float(v[e].y), acc.y);
+                    acc.z = fmaf(w, __uint_as_float(v[e].z), acc.z);
+                    acc.w = fmaf(w, __uint_as_float(v[e].w), acc.w);
+                }
+            }
+            if (h < p.H) {
+                const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+                const __nv_bfloat162 c = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t *>(&a);
+                pk.y = *reinterpret_cast<const uint32_t *>(&c);
+                *reinterpret_cast<uint2 *>(out + (int64_t)h * p.d + dim) = pk;
+            }
+        }
+        cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+    }
+
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -595,6 +717,8 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const MlaP
 
 }  // namespace
 
+int mla_tile_keys() { return kTileKeys; }
+
 int mla_num_splits(int units, int k, int num_sms) {
     const int ntiles = (k + kTileKeys - 1) / kTileKeys;
     if (units <= 0) return 1;
@@ -606,8 +730,10 @@ int mla_num_splits(int units, int k, int num_sms) {
     return splits;
 }
 
+bool mla_cluster_merge(int splits) { return splits > 1 && splits <= kMaxClusterSplits; }
+
 size_t mla_partial_bytes(int units, int splits, int d) {
-    if (splits <= 1) return 0;
+    if (splits <= 1 || mla_cluster_merge(splits)) return 0;
     return (size_t)units * splits * (size_t)(kHeads * d + 2 * kHeads) * sizeof(float);
 }
 
@@ -623,9 +749,24 @@ cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStrea
     }
     const int units = p.B * p.T * p.layers;
     if (units <= 0) return cudaSuccess;
-    cudaError_t e = launch_pdl(sparse_mla_kernel, dim3(units * p.splits), dim3(kThreads), bytes,
-                               stream, maps, p);
-    if (e != cudaSuccess || p.splits == 1) return e;
+    MlaParams q = p;
+    q.cluster = mla_cluster_merge(p.splits) ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units * p.splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = q.cluster ? p.splits : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, maps, q);
+    if (e != cudaSuccess || p.splits == 1 || q.cluster) return e;
     return launch_pdl(mla_combine_kernel, dim3(units * kHeads), dim3(kCombineThreads), 0, stream, p);
 }
 

@@ -49,40 +49,6 @@ __device__ __forceinline__ uint32_t coarse_key(float f) {
     return u >> 5;
 }
 
-// ---- cluster primitives -------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Read a 32-bit word at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t dsmem_ld(const void *local_ptr, uint32_t rank) {
-    uint32_t remote, v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-    return v;
-}
-
-// Read four consecutive 32-bit words (16-byte aligned) from CTA `rank` of the cluster.
-__device__ __forceinline__ uint4 dsmem_ld4(const void *local_ptr, uint32_t rank) {
-    uint32_t remote;
-    uint4 v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
-    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
-}
-
 // ---- shared memory --------------------------------------------------------------------
 
 struct Ctrl {
