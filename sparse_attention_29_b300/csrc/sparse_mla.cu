@@ -21,10 +21,10 @@
 // is the pacing item: one SM moves about 35-40 GB/s of 16-byte cp.async only when many
 // warps issue them from precomputed row addresses, so eight warps do nothing else
 // (row addresses for the next tile are resolved while the current one is in flight).
-// Three more warps issue the MMAs, one thread each (a thread issues a tcgen05.mma about
+// Four more warps issue the MMAs, one thread each (a thread issues a tcgen05.mma about
 // every 55 cycles): two split the S chunks, each into its own accumulator (the softmax
-// adds the two), and one runs the O product, so that O of tile i never waits behind S
-// of tile i+1.  S^T is double-buffered in tensor memory, so S of tile i+1 overlaps the
+// adds the two), and two split the O product's M-blocks, so that O of tile i never
+// waits behind S of tile i+1.  S^T is double-buffered in tensor memory, so S of tile i+1 overlaps the
 // softmax of tile i.
 //
 // Softmax: the M = 64 accumulator puts key 16w + i in TMEM lane 32w + i (w = warp,
@@ -56,8 +56,8 @@ constexpr int kGatherWarp0 = 4;       // warps 4-11: gathers
 constexpr int kGatherThreads = 256;
 constexpr int kMmaWarp = 12;          // S issuer 0 (also owns the tensor memory)
 constexpr int kMmaWarp2 = 13;         // S issuer 1
-constexpr int kQWarp = 14;            // query TMA
-constexpr int kOWarp = 15;            // O issuer
+constexpr int kQWarp = 14;            // query TMA, then O issuer 1
+constexpr int kOWarp = 15;            // O issuer 0
 constexpr int kTileKeys = 64;
 constexpr int kHeads = 64;            // heads padded to 64 (N of both products)
 constexpr int kChunkBytes = kTileKeys * 128;  // 64 dims x 64 keys x 2 B
@@ -92,7 +92,7 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     s.wts = off;  // cluster merge: [split][head] weights
     off += kMaxClusterSplits * kHeads * 4;
     s.bars = off;
-    off += 16 * 8 + 16;
+    off += 50 * 8 + 16;
     s.total = off;
     return s;
 }
@@ -201,16 +201,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *alpha = (float *)(smem + L.alpha);
     float *lsum = (float *)(smem + L.lsum);
     uint64_t *bars = (uint64_t *)(smem + L.bars);
-    uint64_t *full = bars;           // [2] tile buffer landed
-    uint64_t *tfree = bars + 2;      // [2] tile buffer read by both products
-    uint64_t *s_full = bars + 4;     // [2] S^T buffer written
-    uint64_t *s_free = bars + 6;     // [2] S^T buffer read by the softmax
-    uint64_t *p_ready = bars + 8;    // [2] P of the tile in its buffer (and O rescaled)
-    uint64_t *o_done = bars + 10;    // O^T product of a tile complete
-    uint64_t *q_full = bars + 11;
-    uint64_t *drain = bars + 12;
-    volatile int *abort_flag = (volatile int *)(bars + 16);
-    uint32_t *tmem_base_sm = (uint32_t *)(bars + 16) + 1;
+    // chunk-level pipeline: chunk c of a buffer is refilled as soon as the products that
+    // read it are done (latent chunk pair j: O M-block j; rope chunk: P, all of O)
+    uint64_t *full = bars;           // [2][9] chunk c of a buffer landed
+    uint64_t *tfree = bars + 18;     // [2][4] O M-block j of the buffer's tile done
+    uint64_t *tfree_p = bars + 26;   // [2] all of O done: the rope chunk (P) is free
+    uint64_t *s_full = bars + 28;    // [2] S^T buffer written
+    uint64_t *s_free = bars + 30;    // [2] S^T buffer read by the softmax
+    uint64_t *p_ready = bars + 32;   // [2] P of the tile in its buffer (and O rescaled)
+    uint64_t *o_done = bars + 34;    // O^T product of a tile complete
+    uint64_t *q_full = bars + 35;
+    uint64_t *drain = bars + 36;
+    volatile int *abort_flag = (volatile int *)(bars + 48);
+    uint32_t *tmem_base_sm = (uint32_t *)(bars + 48) + 1;
+    int *have_o_sm = (int *)(bars + 49);  // cluster merge: this CTA's O is valid
     const size_t buf_bytes = (size_t)nch * kChunkBytes;
 
     const int tid = threadIdx.x;
@@ -231,6 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_end = min(t_begin + p.tiles_per_split, ntiles_all);
     const int ntiles = max(0, t_end - t_begin);
     const int32_t *idx_row = p.idx + (int64_t)row * p.k;
+    // the gather threads fetch tile 0's token indices now, ahead of the set-up barrier
+    int s_pre = -1;
+    {
+        const int gt = tid - kGatherWarp0 * 32, j = t_begin * kTileKeys + gt;
+        if (gt >= 0 && gt < kTileKeys && ntiles > 0 && j < p.k) s_pre = __ldg(idx_row + j);
+    }
 
     if (tid < kHeads) {
         rn[tid] = -INFINITY;
@@ -238,15 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&full[i], kGatherThreads);
-            mbar_init(&tfree[i], 1);
+            for (int c = 0; c < 9; ++c) mbar_init(&full[i * 9 + c], kGatherThreads);
+            for (int j = 0; j < 4; ++j) mbar_init(&tfree[i * 4 + j], 1);
+            mbar_init(&tfree_p[i], 2);
             mbar_init(&s_full[i], 2);
             mbar_init(&s_free[i], kSoftmaxThreads);
             mbar_init(&p_ready[i], kSoftmaxThreads);
         }
-        mbar_init(o_done, 1);
+        mbar_init(o_done, 2);
         mbar_init(q_full, 1);
-        mbar_init(drain, 3);
+        mbar_init(drain, 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -264,21 +275,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 256;    // nmb x 64 columns
 
     // Roles by warpgroup, each with its register share: the softmax warpgroup holds a
-    // key's logits, probabilities and running sums; the others need few.  512 threads
-    // launch with 128 registers each (65536); after the adjustment 128 x 232 +
-    // 384 x 80 = 60416 are in use.
+    // key's logits, probabilities and running sums; the others need few.  Every
+    // warpgroup returns to 128 before the common tail (the cluster merge).  512 threads
+    // launch with 128 registers each (65536); after the adjustment 128 x 248 +
+    // 384 x 64 = 56320 are in use.
     if (warp >= kMmaWarp) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
-      if (warp == kQWarp) {
-        // ================= query TMA =================
-        if (lane == 0 && ntiles > 0) {
-            const CUtensorMap *qmap = &maps.q[layer];
-            prefetch_tmap(qmap);
-            mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
-            for (int c = 0; c < nch; ++c)
-                tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
-        }
-      } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+      if (warp == kQWarp && lane == 0 && ntiles > 0) {
+        // ================= query TMA (then this warp issues O M-blocks) =================
+        const CUtensorMap *qmap = &maps.q[layer];
+        prefetch_tmap(qmap);
+        mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
+        for (int c = 0; c < nch; ++c)
+            tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
+      }
+      if (warp == kMmaWarp || warp == kMmaWarp2) {
         // ================= S issuers =================
         // issuer r: S chunks [c_lo, c_hi) into its own S^T part
         const int r = warp == kMmaWarp ? 0 : 1;
@@ -290,14 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = ntiles == 0 || mbar_wait(q_full, 0, KID_MLA, abort_flag);
             for (int li = 0; li < ntiles && ok; ++li) {
                 const int bi = li & 1;
-                ok = mbar_wait(&full[bi], (li >> 1) & 1, KID_MLA, abort_flag);
-                if (ok && li >= 2) ok = mbar_wait(&s_free[bi], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
+                if (li >= 2) ok = mbar_wait(&s_free[bi], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
                 if (!ok) break;
-                tc_fence_after();
-                fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
                 const uint32_t tile_a = tiles_a + (uint32_t)(bi * buf_bytes);
                 const uint32_t tSr = tS + (uint32_t)(bi * 2 * kHeads + r * kHeads);
-                for (int c = c_lo; c < c_hi; ++c) {
+                for (int c = c_lo; c < c_hi && ok; ++c) {
+                    ok = mbar_wait(&full[bi * 9 + c], (li >> 1) & 1, KID_MLA, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
@@ -305,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tSr, ad, bd, idS, (c > c_lo || kk > 0) ? 1u : 0u);
                     }
                 }
+                if (!ok) break;
                 mma_commit(&s_full[bi]);
             }
             mma_commit(drain);
@@ -313,8 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-      } else if (warp == kOWarp) {
-        // ================= O issuer: O^T += C^T . P^T once a tile's P is in place ====
+      } else if (warp == kOWarp || warp == kQWarp) {
+        // ============ O issuers: O^T += C^T . P^T once a tile's P is in place ============
+        // issuer r: M-blocks [m_lo, m_hi)
+        const int r = warp == kOWarp ? 0 : 1;
+        const int nmb_a = (nmb + 1) / 2;
+        const int m_lo = r == 0 ? 0 : nmb_a, m_hi = r == 0 ? nmb_a : nmb;
         if (lane == 0) {
             const uint32_t idO = idesc_bf16(128, kHeads, true, true);
             const uint32_t tiles_a = smem_u32(tiles);
@@ -324,15 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t tile_a = tiles_a + (uint32_t)(bi * buf_bytes);
                 const uint32_t p_a = tile_a + rope * kChunkBytes;
-                for (int j = 0; j < nmb; ++j) {
+                for (int j = m_lo; j < m_hi; ++j) {
 #pragma unroll
                     for (int ks = 0; ks < kTileKeys / 16; ++ks) {
                         const uint64_t ad = make_sdesc(tile_a + 2 * j * kChunkBytes + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
                         const uint64_t bd = make_sdesc(p_a + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
                         mma_bf16(tO + j * kHeads, ad, bd, idO, (li > 0 || ks > 0) ? 1u : 0u);
                     }
+                    mma_commit(&tfree[bi * 4 + j]);  // chunks 2j, 2j+1 are free again
                 }
-                mma_commit(&tfree[bi]);
+                mma_commit(&tfree_p[bi]);
                 mma_commit(o_done);
             }
             mma_commit(drain);
@@ -342,16 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 128;\n" ::: "memory");
     } else if (warp >= kGatherWarp0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
         // ================= gathers =================
         const int gt = tid - kGatherWarp0 * 32;
         const uint8_t *kv_bytes = reinterpret_cast<const uint8_t *>(p.kv[layer]);
         const int64_t row_bytes = (int64_t)(p.d + p.r) * 2;
-        auto resolve = [&](int li, int key) -> const uint8_t * {
-            const int j = (t_begin + li) * kTileKeys + key;
-            if (j >= p.k) return nullptr;
-            const int s = __ldg(idx_row + j);
+        auto resolve_s = [&](int s) -> const uint8_t * {
             if (s < 0) return nullptr;
             const int64_t r = resolve_row(p.layout, b, s);
             if (r < 0) {
@@ -360,42 +376,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return kv_bytes + r * row_bytes;
         };
-        if (gt < kTileKeys && ntiles > 0) ptrs[gt] = resolve(0, gt);
+        auto resolve = [&](int li, int key) -> const uint8_t * {
+            const int j = (t_begin + li) * kTileKeys + key;
+            return j < p.k ? resolve_s(__ldg(idx_row + j)) : nullptr;
+        };
+        if (gt < kTileKeys && ntiles > 0) ptrs[gt] = resolve_s(s_pre);
         named_bar_sync(kBarGa, kGatherThreads);
-        // thread gt copies granules q = gt, gt + 256, ... of the tile (q = row * G + gran)
-        const int nq = kTileKeys * G;
-        const int r_start = gt / G, g_start = gt - r_start * G;
-        const int dr = kGatherThreads / G, dg = kGatherThreads - dr * G;
+        // thread gt copies 16-byte granule (gt & 7) of chunk c for rows (gt >> 3) and
+        // (gt >> 3) + 32, chunk by chunk, each chunk as soon as its space is free
+        const int gi = gt & 7, ra = gt >> 3, rb = ra + 32;
         for (int li = 0; li < ntiles; ++li) {
             const int bi = li & 1;
-            if (li >= 2) {
-                const bool got = mbar_wait(&tfree[bi], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
-                if (named_bar_or(kBarGaOr, kGatherThreads, !got)) break;
-            }
             uint8_t *buf = tiles + bi * buf_bytes;
-            const uint8_t *const *pt = ptrs + bi * kTileKeys;
-            int r = r_start, g = g_start;
-#pragma unroll 6
-            for (int q = gt; q < nq; q += kGatherThreads) {
-                const int c = g >> 3, gi = g & 7;
-                const uint8_t *base = pt[r];
-                const bool ok = base != nullptr && (c < nv || gi * 8 < p.r);
-                cp_async_16(buf + c * kChunkBytes + r * 128 + ((gi ^ (r & 7)) << 4),
-                            ok ? base + g * 16 : kv_bytes, ok ? 16u : 0u);
-                g += dg;
-                r += dr;
-                if (g >= G) {
-                    g -= G;
-                    ++r;
+            const uint8_t *pa = ptrs[bi * kTileKeys + ra], *pb = ptrs[bi * kTileKeys + rb];
+            bool fail = false;
+            for (int c = 0; c < nch; ++c) {
+                if (li >= 2 && !fail) {
+                    const uint32_t par = ((li - 2) >> 1) & 1;
+                    if (c == rope) fail = !mbar_wait(&tfree_p[bi], par, KID_MLA, abort_flag);
+                    else if ((c & 1) == 0) fail = !mbar_wait(&tfree[bi * 4 + (c >> 1)], par, KID_MLA, abort_flag);
                 }
+                if (!fail) {
+                    const bool in = c < nv || gi * 8 < p.r;
+                    const int off = c * 128 + gi * 16;
+                    uint8_t *dst = buf + c * kChunkBytes + ((gi ^ (ra & 7)) << 4);
+                    cp_async_16(dst + ra * 128, (in && pa) ? pa + off : kv_bytes, (in && pa) ? 16u : 0u);
+                    cp_async_16(dst + rb * 128, (in && pb) ? pb + off : kv_bytes, (in && pb) ? 16u : 0u);
+                }
+                cp_async_arrive(&full[bi * 9 + c]);
             }
-            cp_async_arrive(&full[bi]);
             if (gt < kTileKeys && li + 1 < ntiles) ptrs[(bi ^ 1) * kTileKeys + gt] = resolve(li + 1, gt);
-            named_bar_sync(kBarGa, kGatherThreads);
+            if (named_bar_or(kBarGaOr, kGatherThreads, fail)) break;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 128;\n" ::: "memory");
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 248;\n" ::: "memory");
         // ================= softmax + epilogue (128 threads) ===============
         // thread: key 16*warp + (lane & 15) of the tile, heads hh*32 .. hh*32+31
         const int key = warp * 16 + (lane & 15);
@@ -423,13 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (named_bar_or(kBarSmOr, kSoftmaxThreads, !got)) { ok = false; break; }
             tc_fence_after();
             const uint32_t taS = tS + lane_addr + (uint32_t)(bi * 2 * kHeads);
-            float x[32];
+            float x[32], t[32];
             tmem_ld_s(taS, x);
+            tc_fence_before();
+            mbar_arrive(&s_free[bi]);
 #pragma unroll
-            for (int h = 0; h < 32; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-            half_transpose_reduce<true>(x, lane);
-            red[warp * 64 + hh * 32 + 2 * (lane & 15)] = x[0];
-            red[warp * 64 + hh * 32 + 2 * (lane & 15) + 1] = x[1];
+            for (int h = 0; h < 32; ++h) {
+                x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+                t[h] = x[h];
+            }
+            half_transpose_reduce<true>(t, lane);
+            red[warp * 64 + hh * 32 + 2 * (lane & 15)] = t[0];
+            red[warp * 64 + hh * 32 + 2 * (lane & 15) + 1] = t[1];
             named_bar_sync(kBarSm, kSoftmaxThreads);
             bool need = false;
             if (tid < kHeads) {
@@ -441,10 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rn[tid] = rnew;
             }
             const bool any = named_bar_or(kBarSmOr, kSoftmaxThreads, need);
-            // probabilities of this key for its 32 heads (S^T is read a second time)
-            tmem_ld_s(taS, x);
-            tc_fence_before();
-            mbar_arrive(&s_free[bi]);
+            // probabilities of this key for its 32 heads
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -452,8 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const float rr = rn[hh * 32 + i + e];
-                    const float lg = x[i + e] * p.scale_log2;
-                    pr[e] = (valid && rr != -INFINITY) ? ex2_approx(lg - rr) : 0.f;
+                    pr[e] = (valid && rr != -INFINITY) ? ex2_approx(x[i + e] - rr) : 0.f;
                 }
                 const __nv_bfloat162 pb = __floats2bfloat162_rn(pr[0], pr[1]);
                 const float2 pf = __bfloat1622float2(pb);
@@ -511,28 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int unit_out = row * p.layers + layer;
         const bool have_o = ok && ntiles > 0;
         if (p.cluster) {
-            // unnormalised O into this CTA's (now idle) tile buffers as [64 heads][d] fp32
-            // (consecutive threads: consecutive dims); rn and lsum stay put.  The cluster
-            // merges them after the next cluster barrier.
-            float *part = reinterpret_cast<float *>(tiles);
-            for (int mb = 0; mb < nmb; ++mb) {
-                const int dim = mb * 128 + kl;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    if (have_o) {
-                        tmem_ld32(tO + lane_addr + mb * kHeads + half * 32, v);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = 0u;
-                    }
-                    if (dim < p.d) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) part[(half * 32 + e) * p.d + dim] = __uint_as_float(v[e]);
-                    }
-                }
-            }
+            // O stays in tensor memory: all warps copy it out for the merge below
+            if (tid == 0) *have_o_sm = have_o ? 1 : 0;
+            tc_fence_before();
         } else if (p.splits == 1) {
             uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
             for (int mb = 0; mb < nmb; ++mb) {
@@ -592,10 +590,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 part[kHeads * p.d + kHeads + kl] = lsum[kl];
             }
         }
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 128;\n" ::: "memory");
     }
 
     if (p.cluster) {
         // ===== merge the cluster's splits: CTA `split` finishes dims [d_lo, d_hi) =====
+        // unnormalised O into this CTA's (now idle) tile buffers as [64 heads][d] fp32 by
+        // all 16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (latent dims), columns
+        // (heads) 16 (w / 4) .. +15; consecutive threads write consecutive dims
+        __syncthreads();  // the softmax warps have seen O complete; rn, lsum final
+        tc_fence_after();
+        {
+            const bool valid_o = *have_o_sm != 0;
+            float *part = reinterpret_cast<float *>(tiles);
+            const int q = warp & 3, cg = warp >> 2;
+            for (int mb = 0; mb < nmb; ++mb) {
+                uint32_t v[16];
+                tmem_ld16(tO + ((uint32_t)(32 * q) << 16) + mb * kHeads + 16 * cg, v);
+                tmem_ld_wait();
+                const int dim = mb * 128 + 32 * q + lane;
+                if (dim < p.d) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        part[(16 * cg + e) * p.d + dim] = valid_o ? __uint_as_float(v[e]) : 0.f;
+                }
+            }
+        }
+        tc_fence_before();
         cluster_sync();  // every CTA's O, maxima (rn) and sums (lsum) are in place
         float *wts = (float *)(smem + L.wts);
         if (tid < kHeads) {
@@ -639,7 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4 v[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    v[e] = s0 + e < p.splits ? dsmem_ld4(src, (uint32_t)(s0 + e)) : make_uint4(0u, 0u, 0u, 0u);
+                    v[e] = s0 + e == split ? *reinterpret_cast<const uint4 *>(src)
+                           : s0 + e < p.splits ? dsmem_ld4(src, (uint32_t)(s0 + e)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float w = wts[(s0 + e) * kHeads + h];
