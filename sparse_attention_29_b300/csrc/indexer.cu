@@ -157,14 +157,15 @@ struct GroupWalk {
 };
 
 // Largest valid position among the rows of query group g (-1 if none).
-__device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool report) {
+__device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool report,
+                                            bool early = false) {
     const int b = g / p.groups_per_seq;
     const int gi = g - b * p.groups_per_seq;
     const int r0 = b * p.T + gi * p.G;
     const int nr = min(p.G, p.T - gi * p.G);
     int maxpos = -1;
     for (int i = 0; i < nr; ++i) {
-        const int pos = __ldg(p.q_pos + r0 + i);
+        const int pos = early ? ldg_early(p.q_pos + r0 + i) : __ldg(p.q_pos + r0 + i);
         if (pos < 0 || pos >= p.Lmax) {
             if (report) record_error(KID_INDEXER, ERR_BAD_POSITION);
             continue;
@@ -210,7 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     griddep_launch_dependents();
-    griddep_wait();  // inputs may come from the previous kernel in the stream
+    // Everything this kernel reads is a step input; only the score stores can conflict
+    // with earlier kernels in the stream (a previous top-k reading the same scores), so
+    // the epilogue warps alone wait for them (griddepcontrol.wait) before their first
+    // store, and the tile list, the query loads and the key stream start at once.  A
+    // kernel that does not trigger its dependents early has completed before this one
+    // starts at all.
 
     // ---- tile list: tiles of each query group, prefix-summed -------------------------
     {
@@ -351,50 +357,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pstage = 0, pslot = 0;
         uint32_t pphase = 0;
         bool ok = true;
+        // ---- lane l resolves tile it0 + l of a batch in two phases: the raw loads (group,
+        // cache page or sequence start, query positions) go out a whole batch ahead, and
+        // the box rows are derived from them after the current batch has been issued ----
+        int f_g = 0, f_newg = 0, f_s0 = 0, f_maxpos = -1, f_pg0 = -1, f_pg1 = -1, f_on = 0;
+        int64_t f_st = 0;
+        auto fetch = [&](int it0) {
+            const int nbf = min(kBatch, ntile - it0);
+            f_on = lane < nbf;
+            if (f_on) {
+                TileCursor c;
+                c.init(prefix, p.num_groups, tb + it0 + lane, te);
+                f_g = c.g;
+                f_newg = c.first_in_range(tb) && (it0 + lane > 0);  // the first is loaded
+                const int b = c.g / p.groups_per_seq;
+                f_s0 = c.j * kTileKeys;
+                if (p.layout.block_table) {
+                    const int lp0 = f_s0 / p.layout.page_size, lp1 = (f_s0 + kBoxRows) / p.layout.page_size;
+                    const int *bt = p.layout.block_table + (int64_t)b * p.layout.pages_per_seq;
+                    f_pg0 = lp0 < p.layout.pages_per_seq ? ldg_early(bt + lp0) : -1;
+                    f_pg1 = lp1 < p.layout.pages_per_seq ? ldg_early(bt + lp1) : -1;
+                } else {
+                    f_st = ldg_early(p.layout.seq_start + b);
+                }
+                f_maxpos = group_maxpos(p, c.g, false, true);
+            }
+        };
+        int l_g = 0, l_newg = 0, l_nbox = 0, l_y0 = 0, l_y1 = 0, l_r0 = -1, l_r1 = -1;
+        auto finish = [&]() {
+            l_g = f_g;
+            l_newg = f_newg;
+            l_nbox = 0;
+            l_y0 = l_y1 = 0;
+            l_r0 = l_r1 = -1;
+            if (!f_on) return;
+            int64_t yb[2];
+            if (p.layout.block_table) {
+                yb[0] = f_pg0 < 0 ? -1 : (int64_t)f_pg0 * p.layout.page_size + f_s0 % p.layout.page_size;
+                yb[1] = f_pg1 < 0 ? -1 : (int64_t)f_pg1 * p.layout.page_size + (f_s0 + kBoxRows) % p.layout.page_size;
+            } else {
+                yb[0] = f_st + f_s0;
+                yb[1] = f_st + f_s0 + kBoxRows;
+            }
+            int ys[2], rs[2];
+            for (int hb = 0; hb < 2; ++hb) {
+                ys[hb] = 0;
+                rs[hb] = -1;
+                if (f_s0 + hb * kBoxRows > f_maxpos) continue;
+                const int64_t y = yb[hb];
+                const bool good = y >= 0 && y < p.layout.num_rows;
+                if (!good) record_error(KID_INDEXER, p.layout.block_table ? ERR_BAD_PAGE : ERR_BAD_INDEX);
+                ys[hb] = good ? (int)y : -2 * kBoxRows;  // wholly outside: TMA fills zeros
+                rs[hb] = good ? (int)y : -1;
+                ++l_nbox;
+            }
+            l_y0 = ys[0];
+            l_y1 = ys[1];
+            l_r0 = rs[0];
+            l_r1 = rs[1];
+        };
+        fetch(0);
+        finish();
         while (ok && it < ntile) {
             const int nb = min(kBatch, ntile - it);
-            // ---- lane l resolves tile it + l: box rows, group start, scale rows ----
-            int l_g = 0, l_newg = 0, l_nbox = 0, l_y0 = 0, l_y1 = 0, l_r0 = -1, l_r1 = -1;
-            if (lane < nb) {
-                TileCursor c;
-                c.init(prefix, p.num_groups, tb + it + lane, te);
-                l_g = c.g;
-                l_newg = c.first_in_range(tb) && (it + lane > 0);  // the first is loaded
-                const int b = c.g / p.groups_per_seq;
-                const int s0 = c.j * kTileKeys;
-                // issue every address load before using any of them
-                int64_t yb[2];
-                if (p.layout.block_table) {
-                    for (int hb = 0; hb < 2; ++hb) {
-                        const int lp = (s0 + hb * kBoxRows) / p.layout.page_size;
-                        const int page = lp < p.layout.pages_per_seq
-                            ? __ldg(p.layout.block_table + (int64_t)b * p.layout.pages_per_seq + lp) : -1;
-                        yb[hb] = page < 0 ? -1
-                                          : (int64_t)page * p.layout.page_size + (s0 + hb * kBoxRows) % p.layout.page_size;
-                    }
-                } else {
-                    const int64_t st = __ldg(p.layout.seq_start + b);
-                    yb[0] = st + s0;
-                    yb[1] = st + s0 + kBoxRows;
-                }
-                const int maxpos = group_maxpos(p, c.g, false);
-                int ys[2], rs[2];
-                for (int hb = 0; hb < 2; ++hb) {
-                    ys[hb] = 0;
-                    rs[hb] = -1;
-                    if (s0 + hb * kBoxRows > maxpos) continue;
-                    const int64_t y = yb[hb];
-                    const bool good = y >= 0 && y < p.layout.num_rows;
-                    if (!good) record_error(KID_INDEXER, p.layout.block_table ? ERR_BAD_PAGE : ERR_BAD_INDEX);
-                    ys[hb] = good ? (int)y : -2 * kBoxRows;  // wholly outside: TMA fills zeros
-                    rs[hb] = good ? (int)y : -1;
-                    ++l_nbox;
-                }
-                l_y0 = ys[0];
-                l_y1 = ys[1];
-                l_r0 = rs[0];
-                l_r1 = rs[1];
-            }
+            if (it + nb < ntile) fetch(it + nb);  // next batch's loads in flight meanwhile
             // ---- issue the batch in order ----
             for (int t = 0; t < nb; ++t, ++it) {
                 const int g = __shfl_sync(0xffffffffu, l_g, t);
@@ -450,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cp_async_arrive(&ksfull[slot]);
                 }
             }
+            finish();
         }
         // drain: every issued copy must land before the CTA's shared memory goes away
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -512,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ================= epilogue =================
+        griddep_wait();  // earlier kernels in the stream are done with the scores
         const int quarter = warp & 3;
         const int eset = (warp - 2) / 4;  // this warp takes tiles it with it % kEpiSets == eset
         const int key_in_tile = quarter * 32 + lane;

@@ -209,6 +209,14 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (TMA, tensor cores).
+// Read-only 32-bit global load issued exactly here (volatile: the compiler may not sink
+// it to the first use, so its latency overlaps the work in between).
+__device__ __forceinline__ int ldg_early(const int *ptr) {
+    int v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
