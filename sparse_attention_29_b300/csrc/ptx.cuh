@@ -407,6 +407,13 @@ __device__ __forceinline__ uint32_t dsmem_ld(const void *local_ptr, uint32_t ran
     return v;
 }
 
+// Write a 32-bit word at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void dsmem_st(void *local_ptr, uint32_t rank, uint32_t v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
 // Four consecutive 32-bit words (16-byte aligned).
 __device__ __forceinline__ uint4 dsmem_ld4(const void *local_ptr, uint32_t rank) {
     uint32_t remote;

@@ -58,12 +58,13 @@ struct Ctrl {
     int found_bin;
     uint32_t found_above;
     uint32_t n_cand;      // B0 candidates in this slice (read by peers)
-    uint32_t n_strict;    // surely selected in this slice (read by peers)
-    uint32_t n_eq;        // keys equal to the threshold in this slice (read by peers)
+    uint32_t n_strict;    // surely selected in this slice
+    uint32_t n_eq;        // keys equal to the threshold in this slice
+    uint32_t peer_st[kMaxCluster], peer_eq[kMaxCluster];  // every slice's counts, pushed
 };
 
 struct Layout {
-    uint32_t vals, bitmap, masks, cand_key, cand_idx, hist, tot, ctrl, total;
+    uint32_t vals, masks, cand_key, cand_idx, hist, tot, ctrl, total;
 };
 
 __host__ __device__ inline Layout topk_layout(int slice_cap) {
@@ -71,9 +72,6 @@ __host__ __device__ inline Layout topk_layout(int slice_cap) {
     uint32_t off = 0;
     L.vals = off;  // the slice starts at its global 16-byte phase: up to 3 floats in
     off += ((uint32_t)slice_cap + 4) * 4;
-    L.bitmap = off;
-    off += ((uint32_t)slice_cap + 31) / 32 * 4;
-    off = (off + 15) & ~15u;
     L.masks = off;  // two ballots per 32 elements
     off += ((uint32_t)slice_cap + 31) / 32 * 8 + 16 * 8;
     off = (off + 15) & ~15u;
@@ -162,7 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const Layout Ly = topk_layout(slice_cap);
     float *vals = reinterpret_cast<float *>(smem_raw + Ly.vals);
-    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem_raw + Ly.bitmap);
     uint32_t *cand_key = reinterpret_cast<uint32_t *>(smem_raw + Ly.cand_key);
     int32_t *cand_idx = reinterpret_cast<int32_t *>(smem_raw + Ly.cand_idx);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem_raw + Ly.hist);  // [2][kBins]
@@ -216,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         for (int i = tid; i < head; i += kThreads) dst[i] = __ldg(src + i);
         for (int i = head + mid + tid; i < m; i += kThreads) dst[i] = __ldg(src + i);
         for (int b = tid; b < 2 * kBins; b += kThreads) hist[b] = 0;
-        for (int w = tid; w < (m + 31) / 32; w += kThreads) bitmap[w] = 0;
+        if (tid == 0) ctrl.n_cand = 0;
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&ctrl.load_bar, 0)) {
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -247,41 +244,49 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
 
     // ---- 2. exact selection inside B0 -------------------------------------------------
     // afterwards: selected = coarse > B0, or coarse == B0 and
-    //   (rank path)  the element's bitmap bit is set;
+    //   (rank path)  it is among the r0 best B0 candidates of the row (its bit is OR-ed
+    //                into the strict selection mask);
     //   (radix path) key > T, or key == T and among the first r_eq such keys of the row.
     const bool all_bin = (r0 == c0);
     const bool rank_path = !all_bin && c0 <= (uint32_t)kCandCap;
     uint32_t T = 0, r_eq = 0;
+    uint32_t *masks_all = reinterpret_cast<uint32_t *>(smem_raw + Ly.masks);  // [m/32][2]
     if (rank_path) {
-        // this slice's B0 candidates, in index order: ballots, per-warp counts, then writes
-        uint32_t nc = 0;
-#pragma unroll 4
-        for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
-            const int i = w_lo + 32 * j + lane;
-            const bool is_c = i < w_hi && coarse_key(vals[i]) == B0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, is_c);
-            if (lane == 0) wmask[2 * j] = bal;
-            nc += __popc(bal);
-        }
-        if (lane == 0) ctrl.warp_st[warp] = nc;
-        __syncthreads();
-        uint32_t slot = 0, mine = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            const uint32_t c = ctrl.warp_st[w];
-            slot += w < warp ? c : 0u;
-            mine += c;
-        }
-        for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
-            const uint32_t bal = wmask[2 * j];
-            if ((bal >> lane) & 1u) {
-                const int i = w_lo + 32 * j + lane;
-                const uint32_t at = slot + __popc(bal & ((1u << lane) - 1u));
-                cand_key[at] = full_key(vals[i]);
-                cand_idx[at] = s_lo + i;
+        // one pass: the strict selections (coarse key above B0) as bit masks in index
+        // order, and this slice's few B0 candidates appended to a list.  Thread t takes
+        // half (t & 1) of 32-element word (t >> 1), reading its 16 elements in an order
+        // rotated by the word index so that a warp's reads hit 32 distinct banks; the two
+        // halves of a word are merged with one shuffle.
+        const int nwords = (m + 31) >> 5;
+        for (int w0 = 0; w0 < nwords; w0 += kThreads / 2) {
+            const int wd = w0 + (tid >> 1), hf = tid & 1;
+            uint32_t st = 0;
+            if (wd < nwords) {
+                const int base = wd * 32 + hf * 16;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int q = (e + wd) & 15;
+                    const int i = base + q;
+                    if (i < m) {
+                        const float f = vals[i];
+                        const uint32_t ck = coarse_key(f);
+                        st |= (ck > B0 ? 1u : 0u) << (hf * 16 + q);
+                        if (ck == B0) {
+                            const uint32_t at = atomicAdd(&ctrl.n_cand, 1u);
+                            cand_key[at] = full_key(f);
+                            cand_idx[at] = s_lo + i;
+                        }
+                    }
+                }
             }
-            slot += __popc(bal);
+            st |= __shfl_xor_sync(0xffffffffu, st, 1);
+            if (wd < nwords && hf == 0) {
+                masks_all[2 * wd] = st;
+                masks_all[2 * wd + 1] = 0u;
+            }
         }
-        if (tid == 0) ctrl.n_cand = mine;
+        __syncthreads();
+        const uint32_t mine = ctrl.n_cand;
         __syncthreads();
         if (csize > 1) cluster_sync();  // every slice's list is complete
         // gather every slice's candidates (tot and hist are free again)
@@ -313,21 +318,32 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
             }
         }
         __syncthreads();
-        // rank this slice's candidates against every candidate of the row: one warp per
-        // candidate, its lanes splitting the comparisons
-        {
-            for (uint32_t c = warp; c < mine; c += kWarps) {
-                const uint32_t key = cand_key[c];
-                const int32_t idx = cand_idx[c];
-                uint32_t better = 0;
-                for (uint32_t j = lane; j < total; j += 32) {
-                    const uint32_t kj = all_key[j];
-                    better += (kj > key) || (kj == key && all_idx[j] < idx);
-                }
-                better = __reduce_add_sync(0xffffffffu, better);
-                if (lane == 0 && better < r0) {
-                    const int li = idx - s_lo;
-                    atomicOr(&bitmap[li >> 5], 1u << (li & 31));
+        // rank this slice's candidates against every candidate of the row: a warp takes
+        // four candidates at a time, its lanes splitting the comparisons (each loaded
+        // entry is compared with all four)
+        for (uint32_t cb = (uint32_t)warp * 4; cb < mine; cb += kWarps * 4) {
+            uint32_t key[4], better[4];
+            int32_t idx[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool v = cb + q < mine;
+                key[q] = v ? cand_key[cb + q] : 0u;
+                idx[q] = v ? cand_idx[cb + q] : 0;
+                better[q] = 0;
+            }
+#pragma unroll 2
+            for (uint32_t j = lane; j < total; j += 32) {
+                const uint32_t kj = all_key[j];
+                const int32_t ij = all_idx[j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) better[q] += (kj > key[q]) || (kj == key[q] && ij < idx[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t bq = __reduce_add_sync(0xffffffffu, better[q]);
+                if (lane == 0 && cb + q < mine && bq < r0) {
+                    const int li = idx[q] - s_lo;
+                    atomicOr(&masks_all[2 * (li >> 5)], 1u << (li & 31));
                 }
             }
         }
@@ -373,8 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         } else if (ck == B0) {
             if (all_bin) {
                 strict = true;
-            } else if (rank_path) {
-                strict = (bitmap[i >> 5] >> (i & 31)) & 1u;
             } else {
                 const uint32_t u = full_key(f);
                 if (u > T) strict = true;
@@ -383,19 +397,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         }
     };
     // per warp segment: selection ballots (strict, equal to the threshold) in index order
+    // (the rank path has them already: strict bits, selected candidates OR-ed in)
+    const int nsteps = (w_hi - w_lo + 31) >> 5;
     uint32_t w_st = 0, w_eq = 0;
+    if (!rank_path) {
 #pragma unroll 4
-    for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
-        const int i = w_lo + 32 * j + lane;
-        bool st = false, eq = false;
-        if (i < w_hi) classify(i, st, eq);
-        const uint32_t bst = __ballot_sync(0xffffffffu, st), beq = __ballot_sync(0xffffffffu, eq);
-        if (lane == 0) {
-            wmask[2 * j] = bst;
-            wmask[2 * j + 1] = beq;
+        for (int j = 0; j < nsteps; ++j) {
+            const int i = w_lo + 32 * j + lane;
+            bool st = false, eq = false;
+            if (i < w_hi) classify(i, st, eq);
+            const uint32_t bst = __ballot_sync(0xffffffffu, st), beq = __ballot_sync(0xffffffffu, eq);
+            if (lane == 0) {
+                wmask[2 * j] = bst;
+                wmask[2 * j + 1] = beq;
+            }
+            w_st += __popc(bst);
+            w_eq += __popc(beq);
         }
-        w_st += __popc(bst);
-        w_eq += __popc(beq);
+    } else {
+        for (int j = lane; j < nsteps; j += 32) w_st += __popc(wmask[2 * j]);
+        w_st = __reduce_add_sync(0xffffffffu, w_st);
     }
     if (lane == 0) {
         ctrl.warp_st[warp] = w_st;
@@ -410,47 +431,93 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         }
         ctrl.n_strict = a;
         ctrl.n_eq = b;
+        // push this slice's counts into every CTA of the cluster (itself included), so
+        // that after the barrier all reads are local and no CTA reads a peer that may
+        // already have finished
+        for (int rr = 0; rr < csize; ++rr) {
+            if (csize > 1) {
+                dsmem_st(&ctrl.peer_st[rank], (uint32_t)rr, a);
+                dsmem_st(&ctrl.peer_eq[rank], (uint32_t)rr, b);
+            } else {
+                ctrl.peer_st[0] = a;
+                ctrl.peer_eq[0] = b;
+            }
+        }
     }
     __syncthreads();
     if (csize > 1) cluster_sync();
     // earlier slices' selections come first; equal keys are taken by ascending index
     uint32_t sel_before = 0, eq_before = 0;
     for (uint32_t rr = 0; rr < rank; ++rr) {
-        const uint32_t s_r = dsmem_ld(&ctrl.n_strict, rr);
-        const uint32_t e_r = dsmem_ld(&ctrl.n_eq, rr);
+        const uint32_t s_r = ctrl.peer_st[rr];
+        const uint32_t e_r = ctrl.peer_eq[rr];
         const uint32_t take = eq_before >= r_eq ? 0u : min(e_r, r_eq - eq_before);
         sel_before += s_r + take;
         eq_before += e_r;
     }
-    if (csize > 1) cluster_sync();  // no CTA leaves while a peer still reads its counters
-    // this warp's offsets: earlier warps' strict selections and taken equal keys
-    uint32_t pos = sel_before, eq_seen = eq_before;
-    for (int w = 0; w < warp; ++w) {
-        const uint32_t e_w = ctrl.warp_eq[w];
-        const uint32_t take = eq_seen >= r_eq ? 0u : min(e_w, r_eq - eq_seen);
-        pos += ctrl.warp_st[w] + take;
-        eq_seen += e_w;
-    }
-    for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
-        const uint32_t bst = wmask[2 * j], beq = wmask[2 * j + 1];
-        uint32_t take = 0;
-        if (beq) {
-            const uint32_t want = eq_seen >= r_eq ? 0u : r_eq - eq_seen;
-            const uint32_t have = __popc(beq);
-            if (want >= have) {
-                take = beq;
-            } else if (want > 0) {
-                const uint32_t cut = __fns(beq, 0, (int)want + 1);  // position of the next one
-                take = beq & ((1u << cut) - 1u);
+    uint32_t pos = sel_before;
+    if (r_eq == 0) {
+        // no equal keys to share out: this warp's offset is a scan over the warps' counts,
+        // and lane l writes the selections of the warp's 32-element word l (+32, ...) on its
+        // own, bit by bit, at that word's offset (a scan over the words' counts)
+        const uint32_t wc = lane < kWarps ? ctrl.warp_st[lane] : 0u;
+        uint32_t winc = wc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, winc, o);
+            if (lane >= o) winc += y;
+        }
+        pos += __shfl_sync(0xffffffffu, winc - wc, warp);
+        for (int j0 = 0; j0 < nsteps; j0 += 32) {
+            const int j = j0 + lane;
+            uint32_t sel = j < nsteps ? wmask[2 * j] : 0u;
+            const uint32_t cnt = __popc(sel);
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
-            eq_seen += have;
+            uint32_t at = pos + incl - cnt;
+            const int ebase = s_lo + w_lo + 32 * j;
+            while (sel) {
+                const int bit = __ffs(sel) - 1;
+                if (at < (uint32_t)k) out[at] = ebase + bit;
+                ++at;
+                sel &= sel - 1u;
+            }
+            pos += __shfl_sync(0xffffffffu, incl, 31);
         }
-        const uint32_t sel = bst | take;
-        if ((sel >> lane) & 1u) {
-            const uint32_t at = pos + __popc(sel & ((1u << lane) - 1u));
-            if (at < (uint32_t)k) out[at] = s_lo + w_lo + 32 * j + lane;
+    } else {
+        // this warp's offsets: earlier warps' strict selections and taken equal keys
+        uint32_t eq_seen = eq_before;
+        for (int w = 0; w < warp; ++w) {
+            const uint32_t e_w = ctrl.warp_eq[w];
+            const uint32_t take = eq_seen >= r_eq ? 0u : min(e_w, r_eq - eq_seen);
+            pos += ctrl.warp_st[w] + take;
+            eq_seen += e_w;
         }
-        pos += __popc(sel);
+        for (int j = 0; w_lo + 32 * j < w_hi; ++j) {
+            const uint32_t bst = wmask[2 * j], beq = wmask[2 * j + 1];
+            uint32_t take = 0;
+            if (beq) {
+                const uint32_t want = eq_seen >= r_eq ? 0u : r_eq - eq_seen;
+                const uint32_t have = __popc(beq);
+                if (want >= have) {
+                    take = beq;
+                } else if (want > 0) {
+                    const uint32_t cut = __fns(beq, 0, (int)want + 1);  // position of the next one
+                    take = beq & ((1u << cut) - 1u);
+                }
+                eq_seen += have;
+            }
+            const uint32_t sel = bst | take;
+            if ((sel >> lane) & 1u) {
+                const uint32_t at = pos + __popc(sel & ((1u << lane) - 1u));
+                if (at < (uint32_t)k) out[at] = s_lo + w_lo + 32 * j + lane;
+            }
+            pos += __popc(sel);
+        }
     }
     // the last warp of the last slice ends at k
     uint32_t sel_base = pos;
