@@ -115,10 +115,7 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
     const int units = B * T * n_layers;
     // the split of a row's keys depends on the rows of one layer only, so that each layer
     // of an IndexShare launch is computed exactly as a separate call would compute it
-    p.splits = mla_num_splits(B * T, k, sms);
-    const int ntiles = (k + mla_tile_keys() - 1) / mla_tile_keys();
-    p.tiles_per_split = (ntiles + p.splits - 1) / p.splits;
-    p.splits = (ntiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    mla_split_plan(B * T, k, sms, d, &p.splits, &p.tiles_per_split);
     const size_t need = mla_partial_bytes(units, p.splits, d);
     if (need) {
         if (!workspace || workspace_bytes < need) return DSA_ERR_WORKSPACE;
@@ -347,10 +344,8 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
     const int sms = current_sm_count();
     if (sms <= 0) return (size_t)-1;
     const int units = B * T * n_layers;
-    int splits = mla_num_splits(B * T, k, sms);
-    const int ntiles = (k + mla_tile_keys() - 1) / mla_tile_keys();
-    const int tps = (ntiles + splits - 1) / splits;
-    splits = (ntiles + tps - 1) / tps;
+    int splits = 1, tps = 1;
+    mla_split_plan(B * T, k, sms, d, &splits, &tps);
     return mla_partial_bytes(units, splits, d);
 }
 

@@ -116,7 +116,8 @@ struct MlaMaps {
 };
 
 int mla_tile_keys();  // keys per sparse MLA tile (the split unit)
-int mla_num_splits(int rows_times_layers, int k, int num_sms);
+// Key splits per (row, layer) and tiles per split for `rows` query rows of one layer.
+void mla_split_plan(int rows, int k, int num_sms, int d, int *splits, int *tiles_per_split);
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
 cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);
 

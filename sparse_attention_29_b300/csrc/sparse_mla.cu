@@ -44,6 +44,8 @@
 // results to the caller's workspace for a combine kernel.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -741,15 +743,68 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const MlaP
 
 int mla_tile_keys() { return kTileKeys; }
 
-int mla_num_splits(int units, int k, int num_sms) {
+// Clusters of `cs` CTAs of the sparse MLA kernel (shared memory for latent width d) that
+// the current device runs at once; cached per device, width and cluster size.
+static int mla_max_clusters(int cs, int d) {
+    constexpr int kDevs = 16;
+    static int cache[kDevs][9][9];  // [device][d / 64][cs], 0: not queried yet
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    const int dd = d / 64;
+    if (dev >= kDevs || dd < 1 || dd > 8 || cs < 1 || cs > kMaxClusterSplits) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int &c = cache[dev][dd][cs];
+    if (c == 0) {
+        const size_t bytes = mla_smem(dd + 1).total + 1024;
+        // the attribute is set to the largest width's need, so that it never drops below
+        // what a launch for another width has already set
+        if (set_smem_attrs(sparse_mla_kernel, (int)(mla_smem(9).total + 1024)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        c = n > 0 ? n : -1;
+    }
+    return c > 0 ? c : 0;
+}
+
+// Split plan of a launch: rows are split only when they are too few to fill the GPU, and
+// when the splits of a row form a cluster, all rows' clusters must run at once (a second
+// wave would double the time), so the split count comes down until they fit.  `units` is
+// the rows of one layer: every layer of an IndexShare launch is split as a separate call
+// would split it.
+void mla_split_plan(int units, int k, int num_sms, int d, int *splits_out, int *tps_out) {
     const int ntiles = (k + kTileKeys - 1) / kTileKeys;
-    if (units <= 0) return 1;
-    // one CTA per SM fits (shared memory); split rows only when there are too few
-    int splits = num_sms / units;
-    if (splits < 1) splits = 1;
-    if (splits > ntiles) splits = ntiles;
-    if (splits > 32) splits = 32;
-    return splits;
+    int s = units > 0 ? num_sms / units : 1;
+    if (s < 1) s = 1;
+    if (s > ntiles) s = ntiles;
+    if (s > 32) s = 32;
+    for (;;) {
+        const int tps = (ntiles + s - 1) / s;
+        const int sf = (ntiles + tps - 1) / tps;
+        if (sf <= 1 || sf > kMaxClusterSplits || units <= mla_max_clusters(sf, d)) {
+            *splits_out = sf;
+            *tps_out = tps;
+            return;
+        }
+        s = sf - 1;
+    }
 }
 
 bool mla_cluster_merge(int splits) { return splits > 1 && splits <= kMaxClusterSplits; }
@@ -765,9 +820,10 @@ cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStrea
     const size_t bytes = L.total + 1024;
     static int attr_bytes = 0;
     if ((int)bytes > attr_bytes) {
-        cudaError_t e = set_smem_attrs(sparse_mla_kernel, (int)bytes);
+        const int max_bytes = (int)(mla_smem(9).total + 1024);  // every width fits
+        cudaError_t e = set_smem_attrs(sparse_mla_kernel, max_bytes);
         if (e != cudaSuccess) return e;
-        attr_bytes = (int)bytes;
+        attr_bytes = max_bytes;
     }
     const int units = p.B * p.T * p.layers;
     if (units <= 0) return cudaSuccess;
