@@ -22,6 +22,8 @@
 // Rows that see at most k tokens skip all of this and write 0..n-1 then -1 padding.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -529,17 +531,63 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
 
 }  // namespace
 
+// Clusters of `cs` CTAs with `bytes` of shared memory each that the current device runs
+// at once (0 if unknown); cached per device, cluster size and shared-memory size.
+static int topk_max_clusters(int cs, int bytes) {
+    constexpr int kDevs = 16, kSlots = 64;
+    struct Entry { int cs, bytes, n; };
+    static Entry cache[kDevs][kSlots];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < kSlots; ++i) {
+        Entry &e = cache[dev][i];
+        if (e.cs == cs && e.bytes == bytes) return e.n;
+        if (e.cs != 0) continue;
+        if (set_smem_attrs(topk_kernel, 227 * 1024) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, topk_kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        e = Entry{cs, bytes, n};
+        return n;
+    }
+    return 0;
+}
+
 // Cluster size and slice capacity of a launch: enough CTAs per row to fill the GPU when
-// rows are few, and to keep every slice within shared memory.
+// rows are few, and to keep every slice within shared memory; a cluster size whose
+// clusters would not all run at once (a second wave) is lowered while the slices still fit.
 static void topk_shape(const TopkParams &p, int num_sms, int &csize, int &slice_cap) {
     constexpr int kSliceMax = 40960;
     const int by_fill = p.rows > 0 ? num_sms / p.rows : 1;
-    const int by_size = (p.Lmax + kSliceMax - 1) / kSliceMax;
+    int by_size = (p.Lmax + kSliceMax - 1) / kSliceMax;
+    if (by_size < 1) by_size = 1;
     csize = by_fill > by_size ? by_fill : by_size;
-    if (csize < 1) csize = 1;
     if (csize > kMaxCluster) csize = kMaxCluster;
-    slice_cap = (p.Lmax + csize - 1) / csize;
-    slice_cap = (slice_cap + 31) & ~31;
+    auto cap_of = [&](int cs) { return (((p.Lmax + cs - 1) / cs) + 31) & ~31; };
+    while (csize > by_size && csize > 1) {
+        const int n = topk_max_clusters(csize, (int)topk_layout(cap_of(csize)).total);
+        if (n <= 0 || p.rows <= n) break;
+        --csize;
+    }
+    slice_cap = cap_of(csize);
 }
 
 cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream) {
@@ -550,9 +598,9 @@ cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream) {
     if (bytes > 227 * 1024) return cudaErrorInvalidValue;
     static int attr_bytes = 0;
     if ((int)bytes > attr_bytes) {
-        cudaError_t e = set_smem_attrs(topk_kernel, (int)bytes);
+        cudaError_t e = set_smem_attrs(topk_kernel, 227 * 1024);  // every slice size fits
         if (e != cudaSuccess) return e;
-        attr_bytes = (int)bytes;
+        attr_bytes = 227 * 1024;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.rows * csize);
