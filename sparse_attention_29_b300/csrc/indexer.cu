@@ -14,13 +14,16 @@
 // The key cache streams through a TMA ring of 128-row tiles (HBM-bound for decode);
 // the query group sits in shared memory (double-buffered across groups).
 //
-// Roles (352 threads): warp 0 produces (it resolves the cache rows of 32 tiles at a time,
-// one lane per tile, then issues the TMA key loads, the query-group loads and cp.async
-// copies of the key scales into a small ring), warps 1 and 10 issue the MMAs of
-// alternate tiles (one elected thread each: the issue loop of one thread, ~1100 cycles
-// per tile, would be slower than the 16 KB per ~750 cycles an SM's share of HBM
-// delivers), warps 2-9 run the epilogue in two sets of four that take alternate tiles
-// (warp w reads TMEM lanes 32*(w%4) .. +31).  Nothing on the per-tile path waits on a
+// Roles (384 threads, three warpgroups): warp 0 produces (it resolves the cache rows of
+// 32 tiles at a time, one lane per tile, then issues the TMA key loads, the query-group
+// loads and cp.async copies of the key scales into a small ring), warps 1 and 2 issue
+// the MMAs of alternate tiles (one elected thread each: the issue loop of one thread,
+// ~1100 cycles per tile, would be slower than the 16 KB per ~750 cycles an SM's share of
+// HBM delivers), warps 4-11 run the epilogue in two sets of four (warp w reads TMEM lanes
+// 32*(w%4) .. +31): in decode the sets take alternate tiles, with several query rows
+// per tile both sets take every tile and split its rows.  The epilogue warpgroups hold
+// a tile's accumulators in registers, so setmaxnreg moves registers to them from the
+// producer warpgroup.  Nothing on the per-tile path waits on a
 // global load.  CTAs are persistent: the tiles of all query groups form one list and
 // each CTA takes a contiguous slice of it, so ragged contexts balance evenly.
 #include "internal.h"
@@ -29,10 +32,26 @@
 namespace dsa {
 namespace {
 
-constexpr int kEpiSets = 2;                     // epilogue warp sets (alternate tiles)
-constexpr int kEpiWarps = 4 * kEpiSets;
-constexpr int kMmaWarps = 2;                    // MMA issuers (alternate tiles): warps 1, 10
-constexpr int kThreads = 32 * (1 + kMmaWarps + kEpiWarps);
+
+constexpr int kMmaWarps = 2;                    // MMA issuers (alternate tiles): warps 1, 2
+// Thread layout.  Warpgroup 0: producer, MMA, MMA, idle; then two epilogue sets of four
+// warps.  Decode (one query row of 64 heads per group): the sets take alternate tiles
+// (the weights stay in registers).  Several rows per group: both sets take every tile,
+// query rows e, e + 2, ... for set e.  (Four sets of one row each were slower.)
+// setmaxnreg moves registers from warpgroup 0 to the epilogue; the shares add up to the
+// pool the block launches with (threads x the per-thread count ptxas gives the kernel).
+template <bool kW64>
+struct EpiCfg {
+    static constexpr int kSets = 2;
+    static constexpr int kWarps = 4 * kSets;
+    static constexpr int kThreads = 32 * (4 + kWarps);
+    static constexpr int kLaunchRegs = 168;  // 65536 / threads, rounded down to 8
+    static constexpr int kRegsControl = 88;
+    static constexpr int kRegsEpilogue = 208;
+    static_assert(128 * kRegsControl + 32 * kWarps * kRegsEpilogue <= kThreads * kLaunchRegs,
+                  "register split");
+    static_assert(kThreads * kLaunchRegs <= 65536, "launch registers");
+};
 constexpr int kTileKeys = 128;
 constexpr int kBoxRows = 64;
 
@@ -178,10 +197,13 @@ __device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool 
 // kW64: decode form (one query row of 64 padded heads per group); its weights stay in
 // registers.  Otherwise they are read from shared memory.
 template <int DI, bool kW64>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap kmap128,
                    const __grid_constant__ CUtensorMap qmap, const IndexerParams p) {
+    constexpr int kThreads = EpiCfg<kW64>::kThreads;
+    constexpr int kEpiSets = EpiCfg<kW64>::kSets;
+    constexpr int kEpiWarps = EpiCfg<kW64>::kWarps;
     constexpr int kTileBytes = kTileKeys * DI;
     constexpr uint32_t kLayout = DI == 128 ? kLayoutSW128 : (DI == 64 ? kLayoutSW64 : kLayoutSW32);
     constexpr uint32_t kSBO = 8 * DI;
@@ -277,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < p.num_acc; ++i) {
             mbar_init(&accfull[i], 1);
-            mbar_init(&accempty[i], 4);
+            mbar_init(&accempty[i], kW64 ? 4 : kEpiWarps);  // the warps that read it
         }
         for (int i = 0; i < L.ring; ++i) mbar_init(&ksfull[i], 32);  // every producer lane
         mbar_init(drain, kMmaWarps);
@@ -298,9 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_base_sm;
 
-    const bool mma_warp = (warp == 1 || warp >= 2 + kEpiWarps);
-    const int mma_rank = warp == 1 ? 0 : warp - (1 + kEpiWarps);  // 0 .. kMmaWarps-1
-    if (warp == 0) {
+    const bool mma_warp = (warp == 1 || warp == 2);
+    const int mma_rank = warp - 1;  // 0 .. kMmaWarps-1
+    if (warp < 4) {
+      if constexpr (EpiCfg<kW64>::kRegsControl < EpiCfg<kW64>::kLaunchRegs)
+          asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(EpiCfg<kW64>::kRegsControl) : "memory");
+      if (warp == 0) {
         // ================= producer =================
         // query group g -> slot: q codes by TMA (rows n = qi*HP + h) when the heads need no
         // padding, else plain loads with zero rows; weights * q_scale and positions by the
@@ -537,11 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+      }
+      // warp 3 has no role
     } else {
+        if constexpr (EpiCfg<kW64>::kRegsEpilogue > EpiCfg<kW64>::kLaunchRegs)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(EpiCfg<kW64>::kRegsEpilogue) : "memory");
         // ================= epilogue =================
         griddep_wait();  // earlier kernels in the stream are done with the scores
         const int quarter = warp & 3;
-        const int eset = (warp - 2) / 4;  // this warp takes tiles it with it % kEpiSets == eset
+        const int eset = (warp - 4) / 4;  // set e: warps 4e+4 .. 4e+7
         const int key_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         float wr[kW64 ? 64 : 1];
@@ -573,7 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if ((it & (kEpiSets - 1)) == eset) {
+            // decode: the two sets take alternate tiles; several query rows per tile: every
+            // set takes every tile, query rows eset, eset + kEpiSets, ...
+            if (!kW64 || (it & (kEpiSets - 1)) == eset) {
                 const bool got = mbar_wait(&accfull[abuf], aphase, KID_INDEXER, abort_flag) &&
                                  mbar_wait(&ksfull[kslot], ksphase, KID_INDEXER, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) break;
@@ -598,33 +629,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (s <= pos[0])
                         p.scores[(int64_t)r0 * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
                 } else {
+                    // both sets work on every tile: set e takes query rows 2e and 2e+1, and
+                    // both rows' accumulators are loaded before one wait (tcgen05.wait::ld
+                    // covers every outstanding load); four independent chains per row
                     const float *wq = wbuf + slot * p.N;
-                    for (int qi = 0; qi < nr; ++qi) {
-                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
-                        for (int c0 = 0; c0 < p.HP; c0 += 64) {
-                            uint32_t v[4][16];
-                            const int nchunk = min(4, (p.HP - c0) / 16);
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                if (c < nchunk) tmem_ld16(tacc + (uint32_t)(qi * p.HP + c0 + c * 16), v[c]);
+                    if (p.HP == 64) {
+                        // this set's rows one at a time: one 64-column load and wait each
+                        for (int q = eset; q < nr; q += kEpiSets) {
+                            uint32_t v0[64];
+                            tmem_ld32(tacc + (uint32_t)(q * 64), *reinterpret_cast<uint32_t (*)[32]>(&v0[0]));
+                            tmem_ld32(tacc + (uint32_t)(q * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&v0[32]));
                             tmem_ld_wait();
+                            const float4 *w0 = (const float4 *)(wq + q * 64);
+                            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                if (c < nchunk) {
-                                    const float4 *w4 = (const float4 *)(wq + qi * p.HP + c0 + c * 16);
+                            for (int h = 0; h < 64; h += 4) {
+                                const float4 ww = w0[h >> 2];
+                                a0 = fmaf(ww.x, fmaxf(__uint_as_float(v0[h + 0]), 0.f), a0);
+                                a1 = fmaf(ww.y, fmaxf(__uint_as_float(v0[h + 1]), 0.f), a1);
+                                a2 = fmaf(ww.z, fmaxf(__uint_as_float(v0[h + 2]), 0.f), a2);
+                                a3 = fmaf(ww.w, fmaxf(__uint_as_float(v0[h + 3]), 0.f), a3);
+                            }
+                            if (s <= pos[q]) p.scores[(int64_t)(r0 + q) * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
+                        }
+                    } else {
+                        // other head counts: this set's rows one at a time, 32 heads per
+                        // load (then 16 for the rest; HP is a multiple of 16)
+                        for (int q = eset; q < nr; q += kEpiSets) {
+                            float a0 = 0.f, a1 = 0.f;
+                            int c0 = 0;
+                            for (; c0 + 32 <= p.HP; c0 += 32) {
+                                uint32_t v[32];
+                                tmem_ld32(tacc + (uint32_t)(q * p.HP + c0), v);
+                                tmem_ld_wait();
+                                const float *wr = wq + q * p.HP + c0;
 #pragma unroll
-                                    for (int e4 = 0; e4 < 4; ++e4) {
-                                        const float4 ww = w4[e4];
-                                        a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[c][e4 * 4 + 0]), 0.f), a0);
-                                        a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[c][e4 * 4 + 1]), 0.f), a1);
-                                        a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[c][e4 * 4 + 2]), 0.f), a2);
-                                        a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[c][e4 * 4 + 3]), 0.f), a3);
-                                    }
+                                for (int e = 0; e < 32; e += 2) {
+                                    a0 = fmaf(wr[e], fmaxf(__uint_as_float(v[e]), 0.f), a0);
+                                    a1 = fmaf(wr[e + 1], fmaxf(__uint_as_float(v[e + 1]), 0.f), a1);
                                 }
                             }
+                            if (c0 < p.HP) {
+                                uint32_t v[16];
+                                tmem_ld16(tacc + (uint32_t)(q * p.HP + c0), v);
+                                tmem_ld_wait();
+                                const float *wr = wq + q * p.HP + c0;
+#pragma unroll
+                                for (int e = 0; e < 16; e += 2) {
+                                    a0 = fmaf(wr[e], fmaxf(__uint_as_float(v[e]), 0.f), a0);
+                                    a1 = fmaf(wr[e + 1], fmaxf(__uint_as_float(v[e + 1]), 0.f), a1);
+                                }
+                            }
+                            if (s <= pos[q]) p.scores[(int64_t)(r0 + q) * p.Lmax + s] = (a0 + a1) * ksc;
                         }
-                        if (s <= pos[qi])
-                            p.scores[(int64_t)(r0 + qi) * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
                     }
                 }
                 tc_fence_before();
@@ -658,7 +715,7 @@ cudaError_t launch_di(const IndexerParams &p, const CUtensorMap &kmap,
         if (e != cudaSuccess) return e;
         attr_set_bytes = (int)bytes;
     }
-    return launch_pdl(indexer_kernel<DI, kW64>, dim3(grid), dim3(kThreads), bytes, stream, kmap,
+    return launch_pdl(indexer_kernel<DI, kW64>, dim3(grid), dim3(EpiCfg<kW64>::kThreads), bytes, stream, kmap,
                       kmap128, qmap, p);
 }
 
