@@ -38,10 +38,11 @@
 //
 // Rows with few keys are split over several CTAs (split-KV), merged with the log-sum-exp
 // rule.  Up to kMaxClusterSplits splits of a row run as one thread-block cluster: each CTA
-// leaves its unnormalised O, running maxima and sums in its shared memory and every CTA
-// then finishes a slice of the latent dims from all of them through distributed shared
-// memory (no global round trip, no second kernel).  More splits than that write partial
-// results to the caller's workspace for a combine kernel.
+// writes its unnormalised O to the workspace and keeps its running maxima and sums in
+// shared memory; after one cluster barrier every CTA finishes a slice of the latent dims
+// from all splits (the partials come back from L2, the maxima and sums through
+// distributed shared memory) -- no second kernel.  More splits than that write partial
+// results for a combine kernel.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -597,29 +598,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (p.cluster) {
         // ===== merge the cluster's splits: CTA `split` finishes dims [d_lo, d_hi) =====
-        // unnormalised O into this CTA's (now idle) tile buffers as [64 heads][d] fp32 by
-        // all 16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (latent dims), columns
-        // (heads) 16 (w / 4) .. +15; consecutive threads write consecutive dims
+        // The unnormalised O goes to this split's slot of the workspace as [64 heads][d]
+        // bf16 (all 16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31, the latent dims,
+        // columns 16 (w / 4) .. +15, the heads; consecutive threads store consecutive
+        // dims); after the cluster barrier each CTA reads its slice of every split back
+        // from L2.  The exchange is L2-bandwidth-bound, so it moves bf16: one more
+        // rounding (relative 2^-9) ahead of a four-term weighted sum whose result is
+        // rounded to bf16 anyway.  The maxima and sums (rn, lsum) stay in shared memory.
+        const size_t stride = (size_t)(kHeads * p.d + 2 * kHeads);
+        const int unit_out = row * p.layers + layer;
+        float *part_base = p.partial + (int64_t)unit_out * p.splits * stride;
         __syncthreads();  // the softmax warps have seen O complete; rn, lsum final
         tc_fence_after();
         {
             const bool valid_o = *have_o_sm != 0;
-            float *part = reinterpret_cast<float *>(tiles);
+            uint16_t *part = reinterpret_cast<uint16_t *>(part_base + (size_t)split * stride);
             const int q = warp & 3, cg = warp >> 2;
-            for (int mb = 0; mb < nmb; ++mb) {
-                uint32_t v[16];
-                tmem_ld16(tO + ((uint32_t)(32 * q) << 16) + mb * kHeads + 16 * cg, v);
-                tmem_ld_wait();
+            // every M-block's 16 columns are loaded before one wait
+            uint32_t v[4][16];
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb)
+                if (mb < nmb) tmem_ld16(tO + ((uint32_t)(32 * q) << 16) + mb * kHeads + 16 * cg, v[mb]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb) {
                 const int dim = mb * 128 + 32 * q + lane;
-                if (dim < p.d) {
+                if (mb < nmb && dim < p.d) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        part[(16 * cg + e) * p.d + dim] = valid_o ? __uint_as_float(v[e]) : 0.f;
+                        part[(int64_t)(16 * cg + e) * p.d + dim] =
+                            valid_o ? __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[mb][e]))) : (uint16_t)0;
                 }
             }
         }
         tc_fence_before();
-        cluster_sync();  // every CTA's O, maxima (rn) and sums (lsum) are in place
+        __threadfence();
+        cluster_sync();  // every split's O (global), maxima and sums (shared) are in place
         float *wts = (float *)(smem + L.wts);
         if (tid < kHeads) {
             // every split's maximum and sum for head h, all loads in flight at once
@@ -650,27 +664,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ds = ((p.d + p.splits - 1) / p.splits + 3) & ~3;
         const int d_lo = min(p.d, split * ds), d_hi = min(p.d, d_lo + ds);
         const int ng = (d_hi - d_lo) >> 2;  // groups of 4 dims
-        const float *part = reinterpret_cast<const float *>(tiles);
         uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
+#pragma unroll 2
         for (int it = tid; it < ng * kHeads; it += kThreads) {
             const int h = it / ng, dim = d_lo + 4 * (it - h * ng);  // consecutive threads: dims
-            const float *src = part + h * p.d + dim;
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(part_base) + (int64_t)h * p.d + dim;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int s0 = 0; s0 < kMaxClusterSplits; s0 += 4) {
                 if (s0 >= p.splits) break;
-                uint4 v[4];
+                uint2 v[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    v[e] = s0 + e == split ? *reinterpret_cast<const uint4 *>(src)
-                           : s0 + e < p.splits ? dsmem_ld4(src, (uint32_t)(s0 + e)) : make_uint4(0u, 0u, 0u, 0u);
+                    v[e] = s0 + e < p.splits
+                               ? __ldcg(reinterpret_cast<const uint2 *>(src + (size_t)(s0 + e) * stride * 2))
+                               : make_uint2(0u, 0u);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float w = wts[(s0 + e) * kHeads + h];
-                    acc.x = fmaf(w, __uint_as_float(v[e].x), acc.x);
-                    acc.y = fmaf(w, __uint_as_float(v[e].y), acc.y);
-                    acc.z = fmaf(w, __uint_as_float(v[e].z), acc.z);
-                    acc.w = fmaf(w, __uint_as_float(v[e].w), acc.w);
+                    acc.x = fmaf(w, __uint_as_float(v[e].x << 16), acc.x);
+                    acc.y = fmaf(w, __uint_as_float(v[e].x & 0xFFFF0000u), acc.y);
+                    acc.z = fmaf(w, __uint_as_float(v[e].y << 16), acc.z);
+                    acc.w = fmaf(w, __uint_as_float(v[e].y & 0xFFFF0000u), acc.w);
                 }
             }
             if (h < p.H) {
@@ -682,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint2 *>(out + (int64_t)h * p.d + dim) = pk;
             }
         }
-        cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+        cluster_sync();  // no CTA leaves while a peer may still read its maxima and sums
     }
 
     tc_fence_before();
@@ -810,7 +825,7 @@ void mla_split_plan(int units, int k, int num_sms, int d, int *splits_out, int *
 bool mla_cluster_merge(int splits) { return splits > 1 && splits <= kMaxClusterSplits; }
 
 size_t mla_partial_bytes(int units, int splits, int d) {
-    if (splits <= 1 || mla_cluster_merge(splits)) return 0;
+    if (splits <= 1) return 0;
     return (size_t)units * splits * (size_t)(kHeads * d + 2 * kHeads) * sizeof(float);
 }
 

@@ -40,7 +40,7 @@ def _random_idx(case, seed, frac_invalid=0.02):
 
 @pytest.mark.parametrize("lengths,k,splits", [
     ([5000, 3000, 2100], 2048, True),   # three rows: more splits than a cluster holds
-    ([2500] * 32, 2048, False),         # 32 rows x 4 splits, merged in a cluster
+    ([2500] * 32, 2048, True),          # 32 rows x 4 splits, merged in a cluster through the scratch
     ([700] * 150, 512, False),          # more rows than SMs: no split, no scratch used
 ])
 def test_noalloc_decode_matches_workspace_entry(lengths, k, splits):
