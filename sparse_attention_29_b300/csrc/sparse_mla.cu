@@ -11,10 +11,10 @@
 // cp.async in 16-byte granules into shared memory in the tensor cores' 128-byte-swizzled
 // layout: chunk c of a tile holds dims 64c..64c+63 of its 64 rows.  That one layout
 // serves both products:
-//   S^T[key, head]  = C[key, :] . Q[head, :]      A = C (K-major), B = Q (K-major)
-//   O^T[dim, head] += C[key, dim]^T P^T[key, head] A = C^T (MN-major), B = P^T (MN-major)
-// S^T runs as M = 64 tcgen05 MMAs (keys on M), O^T as M = 128 MMAs (latent dims on M),
-// both with the 64 heads on N and fp32 accumulators in tensor memory.
+//   S[head, key]    = Q[head, :] . C[key, :]       A = Q (K-major), B = C (K-major)
+//   O^T[dim, head] += C[key, dim]^T P^T[key, head] A = C^T (MN-major), B = P (K-major)
+// S runs as M = 64 tcgen05 MMAs (heads on M, keys on N), O^T as M = 128 MMAs (latent
+// dims on M, heads on N), fp32 accumulators in tensor memory.
 //
 // The query (64 heads x 576 x 2 B = 72 KB) and two tiles (2 x 72 KB) fill shared memory,
 // so tile i+1 is gathered while tile i is in the products and the softmax.  The gather
@@ -27,12 +27,12 @@
 // waits behind S of tile i+1.  S^T is double-buffered in tensor memory, so S of tile i+1 overlaps the
 // softmax of tile i.
 //
-// Softmax: the M = 64 accumulator puts key 16w + i in TMEM lane 32w + i (w = warp,
-// i < 16); a 16x32bx2 tcgen05.ld hands thread i < 16 of warp w heads 0-31 of that key
-// and thread 16 + i heads 32-63, so all 128 softmax threads work.  Per-head maxima are
-// reduced over the tile's 64 keys with a transposing butterfly over 16 lanes, then
-// across the four warps.  The probabilities are written (bf16) over the tile's rope
-// chunk, which S no longer needs.  Online softmax rescales O in tensor memory only when
+// Softmax: the M = 64 accumulator puts head 16w + i in TMEM lane 32w + i (w = warp,
+// i < 16); a 16x32bx2 tcgen05.ld hands thread i < 16 of warp w keys 0-31 of that head
+// and thread 16 + i keys 32-63, so all 128 softmax threads work and a head's maximum
+// and sum over the tile are one thread's plus one shuffle.  The probabilities are
+// written (bf16, one 128-byte row of 64 keys per head) over the tile's rope chunk,
+// which S no longer needs.  Online softmax rescales O in tensor memory only when
 // a head's running maximum grows by more than 2^8 (the result is the same; the
 // unnormalised terms just stay < 2^8).
 //
@@ -72,7 +72,7 @@ constexpr int kMaxClusterSplits = 8;          // portable cluster size
 constexpr int kBarSm = 1, kBarSmOr = 2, kBarGa = 3, kBarGaOr = 4;
 
 struct MlaSmem {
-    uint32_t q, tile, ptrs, red, rn, alpha, lsum, wts, bars, total;
+    uint32_t q, tile, ptrs, rn, alpha, lsum, wts, vm, bars, total;
 };
 
 __host__ __device__ inline MlaSmem mla_smem(int nch) {
@@ -84,8 +84,6 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     off += 2u * (uint32_t)nch * kChunkBytes;
     s.ptrs = off;  // [2][64] row addresses
     off += 2 * kTileKeys * 8;
-    s.red = off;
-    off += 4 * kHeads * 4;
     s.rn = off;
     off += kHeads * 4;
     s.alpha = off;
@@ -94,15 +92,12 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     off += kHeads * 4;
     s.wts = off;  // cluster merge: [split][head] weights
     off += kMaxClusterSplits * kHeads * 4;
+    s.vm = off;  // [2 buffers][2] key-validity words of a tile
+    off += 16;
     s.bars = off;
     off += 50 * 8 + 16;
     s.total = off;
     return s;
-}
-
-__device__ __forceinline__ uint32_t swz128(int row, int gran) {
-    const uint32_t lin = (uint32_t)row * 128 + (uint32_t)gran * 16;
-    return lin ^ (((lin >> 7) & 7u) << 4);
 }
 
 // Physical cache row of token s of sequence b, or -1 if s or the layout entry is invalid.
@@ -119,44 +114,6 @@ __device__ __forceinline__ int64_t resolve_row(const CacheLayout &L, int b, int 
         row = (int64_t)L.seq_start[b] + s;
     }
     return (row >= 0 && row < L.num_rows) ? row : -1;
-}
-
-// Transposing butterfly over 32 lanes: on entry x[0..63] are one key's values for heads
-// 0..63; on exit x[0], x[1] hold heads 2*lane, 2*lane+1 combined over the warp's keys.
-template <bool kMax>
-__device__ __forceinline__ void warp_transpose_reduce(float (&x)[64], int lane) {
-#pragma unroll
-    for (int step = 0; step < 5; ++step) {
-        const int half = 32 >> step;
-        const int off = 16 >> step;
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? x[i] : x[i + half];
-            const float keep = upper ? x[i + half] : x[i];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            x[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-}
-
-// The same over the 16 lanes of each half-warp with 32 values (heads of one half): on
-// exit x[0], x[1] hold heads 2*(lane & 15), +1 of the half, combined over its 16 keys.
-template <bool kMax>
-__device__ __forceinline__ void half_transpose_reduce(float (&x)[32], int lane) {
-#pragma unroll
-    for (int step = 0; step < 4; ++step) {
-        const int half = 16 >> step;
-        const int off = 8 >> step;
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? x[i] : x[i + half];
-            const float keep = upper ? x[i + half] : x[i];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-            x[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
 }
 
 // 16x32bx2 load of 32 columns: thread i < 16 of the warp reads TMEM lane (base + i),
@@ -191,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nch = nv + 1;              // + the rope chunk
     const int nmb = (nv + 1) / 2;        // M-blocks of the O product (128 dims each)
     const int rope = nv;                 // index of the rope chunk (later: P)
-    const int G = nch * 8;               // 16-byte granules per gathered row
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -199,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *qs = smem + L.q;
     uint8_t *tiles = smem + L.tile;
     const uint8_t **ptrs = (const uint8_t **)(smem + L.ptrs);  // [2][64], null: invalid
-    float *red = (float *)(smem + L.red);
+    uint32_t *vm = (uint32_t *)(smem + L.vm);
     float *rn = (float *)(smem + L.rn);
     float *alpha = (float *)(smem + L.alpha);
     float *lsum = (float *)(smem + L.lsum);
@@ -280,10 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Roles by warpgroup, each with its register share: the softmax warpgroup holds a
     // key's logits, probabilities and running sums; the others need few.  Every
     // warpgroup returns to 128 before the common tail (the cluster merge).  512 threads
-    // launch with 128 registers each (65536); after the adjustment 128 x 248 +
-    // 384 x 64 = 56320 are in use.
+    // launch with 128 registers each (65536); after the adjustment 128 x 168 +
+    // 384 x 88 = 55296 are in use.
     if (warp >= kMmaWarp) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
       if (warp == kQWarp && lane == 0 && ntiles > 0) {
         // ================= query TMA (then this warp issues O M-blocks) =================
         const CUtensorMap *qmap = &maps.q[layer];
@@ -299,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nch_a = (nch + 1) / 2;
         const int c_lo = r == 0 ? 0 : nch_a, c_hi = r == 0 ? nch_a : nch;
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16(64, kHeads, false, false);
+            const uint32_t idS = idesc_bf16(kHeads, kTileKeys, false, false);
             const uint32_t tiles_a = smem_u32(tiles), q_a = smem_u32(qs);
             bool ok = ntiles == 0 || mbar_wait(q_full, 0, KID_MLA, abort_flag);
             for (int li = 0; li < ntiles && ok; ++li) {
@@ -315,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
-                        const uint64_t bd = make_sdesc(q_a + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
+                        const uint64_t ad = make_sdesc(q_a + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
+                        const uint64_t bd = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
                         mma_bf16(tSr, ad, bd, idS, (c > c_lo || kk > 0) ? 1u : 0u);
                     }
                 }
@@ -336,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nmb_a = (nmb + 1) / 2;
         const int m_lo = r == 0 ? 0 : nmb_a, m_hi = r == 0 ? nmb_a : nmb;
         if (lane == 0) {
-            const uint32_t idO = idesc_bf16(128, kHeads, true, true);
+            const uint32_t idO = idesc_bf16(128, kHeads, true, false);
             const uint32_t tiles_a = smem_u32(tiles);
             for (int li = 0; li < ntiles; ++li) {
                 const int bi = li & 1;
@@ -348,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int ks = 0; ks < kTileKeys / 16; ++ks) {
                         const uint64_t ad = make_sdesc(tile_a + 2 * j * kChunkBytes + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
-                        const uint64_t bd = make_sdesc(p_a + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
+                        const uint64_t bd = make_sdesc(p_a + ks * 32, 16, 1024, kLayoutSW128);
                         mma_bf16(tO + j * kHeads, ad, bd, idO, (li > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(&tfree[bi * 4 + j]);  // chunks 2j, 2j+1 are free again
@@ -365,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("setmaxnreg.inc.sync.aligned.u32 128;\n" ::: "memory");
     } else if (warp >= kGatherWarp0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
         // ================= gathers =================
         const int gt = tid - kGatherWarp0 * 32;
         const uint8_t *kv_bytes = reinterpret_cast<const uint8_t *>(p.kv[layer]);
@@ -414,78 +370,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("cp.async.wait_all;" ::: "memory");
         asm volatile("setmaxnreg.inc.sync.aligned.u32 128;\n" ::: "memory");
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 248;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 168;\n" ::: "memory");
         // ================= softmax + epilogue (128 threads) ===============
-        // thread: key 16*warp + (lane & 15) of the tile, heads hh*32 .. hh*32+31
-        const int key = warp * 16 + (lane & 15);
-        const int hh = lane >> 4;
+        // The M = 64 accumulator of S puts head 16w + i in TMEM lane 32w + i (i < 16):
+        // thread i < 16 of warp w takes head 16w + i, keys 0-31 of the tile, thread 16 + i
+        // the same head, keys 32-63.  Maxima and sums are per thread plus one shuffle.
+        const int hrow = warp * 16 + (lane & 15);
+        const int kh = lane >> 4;
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        float lp[32];
-#pragma unroll
-        for (int h = 0; h < 32; ++h) lp[h] = 0.f;
-        // validity of this thread's key in tile li (same rule as the gathers)
-        auto key_valid = [&](int li) -> bool {
+        float rmax = -INFINITY;  // running maximum of this head (log2 units)
+        float lpart = 0.f;       // running sum of this thread's probabilities
+        // validity of key `key` of tile li (same rule as the gathers)
+        auto key_valid = [&](int li, int key) -> bool {
             const int j = (t_begin + li) * kTileKeys + key;
             if (li >= ntiles || j >= p.k) return false;
             const int s = __ldg(idx_row + j);
             return s >= 0 && resolve_row(p.layout, b, s) >= 0;
         };
+        if (warp == 0) {
+            const uint32_t m0 = __ballot_sync(0xffffffffu, key_valid(0, lane));
+            const uint32_t m1 = __ballot_sync(0xffffffffu, key_valid(0, lane + 32));
+            if (lane == 0) {
+                vm[0] = m0;
+                vm[1] = m1;
+            }
+        }
+        named_bar_sync(kBarSm, kSoftmaxThreads);
         bool ok = true;
-        bool valid_next = key_valid(0);
         for (int li = 0; li < ntiles && ok; ++li) {
             const int bi = li & 1;
-            const bool valid = valid_next;
-            valid_next = key_valid(li + 1);
+            // warp 0 finds the next tile's valid keys (its loads overlap the wait below)
+            bool vn0 = false, vn1 = false;
+            if (warp == 0) {
+                vn0 = key_valid(li + 1, lane);
+                vn1 = key_valid(li + 1, lane + 32);
+            }
             // every decision that guards a named barrier or a warp-collective TMEM access
             // is made uniform over the 128 threads first
             const bool got = mbar_wait(&s_full[bi], (li >> 1) & 1, KID_MLA, abort_flag);
             if (named_bar_or(kBarSmOr, kSoftmaxThreads, !got)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t taS = tS + lane_addr + (uint32_t)(bi * 2 * kHeads);
-            float x[32], t[32];
+            const uint32_t taS = tS + lane_addr + (uint32_t)(bi * 2 * kTileKeys);
+            float x[32];
             tmem_ld_s(taS, x);
             tc_fence_before();
             mbar_arrive(&s_free[bi]);
+            const uint32_t vmask = vm[2 * bi + kh];
+            float m = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-                t[h] = x[h];
+            for (int e = 0; e < 32; ++e) {
+                x[e] = ((vmask >> e) & 1u) ? x[e] * p.scale_log2 : -INFINITY;
+                m = fmaxf(m, x[e]);
             }
-            half_transpose_reduce<true>(t, lane);
-            red[warp * 64 + hh * 32 + 2 * (lane & 15)] = t[0];
-            red[warp * 64 + hh * 32 + 2 * (lane & 15) + 1] = t[1];
-            named_bar_sync(kBarSm, kSoftmaxThreads);
-            bool need = false;
-            if (tid < kHeads) {
-                const float m = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-                const float rold = rn[tid];
-                need = m > rold + kRescaleLog2;
-                const float rnew = need ? m : rold;
-                alpha[tid] = need ? ex2_approx(rold - rnew) : 1.f;
-                rn[tid] = rnew;
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            const bool need = m > rmax + kRescaleLog2;
+            const float rnew = need ? m : rmax;
+            const float al = need ? ex2_approx(rmax - rnew) : 1.f;
+            rmax = rnew;
+            if (kh == 0) alpha[hrow] = al;
+            if (warp == 0) {
+                const uint32_t m0 = __ballot_sync(0xffffffffu, vn0);
+                const uint32_t m1 = __ballot_sync(0xffffffffu, vn1);
+                if (lane == 0) {
+                    vm[2 * (bi ^ 1)] = m0;
+                    vm[2 * (bi ^ 1) + 1] = m1;
+                }
             }
             const bool any = named_bar_or(kBarSmOr, kSoftmaxThreads, need);
-            // probabilities of this key for its 32 heads
-            uint32_t pk[16];
+            // probabilities of this head for its 32 keys; the sum takes the rounded values.
+            // P^T goes over the tile's rope chunk, K-major: head h's 64 keys in one
+            // 128-byte row (128-byte swizzle), keys 8g..8g+7 in 16-byte granule g.
+            uint8_t *prow = tiles + bi * buf_bytes + rope * kChunkBytes + hrow * 128;
+            float ps = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                float pr[2];
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pk[4];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float rr = rn[hh * 32 + i + e];
-                    pr[e] = (valid && rr != -INFINITY) ? ex2_approx(x[i + e] - rr) : 0.f;
+                for (int e = 0; e < 8; e += 2) {
+                    const int i = 8 * q + e;
+                    const float p0 = rmax != -INFINITY ? ex2_approx(x[i] - rmax) : 0.f;
+                    const float p1 = rmax != -INFINITY ? ex2_approx(x[i + 1] - rmax) : 0.f;
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    const float2 pf = __bfloat1622float2(pb);
+                    ps += pf.x + pf.y;
+                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
                 }
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(pr[0], pr[1]);
-                const float2 pf = __bfloat1622float2(pb);
-                lp[i] = fmaf(lp[i], alpha[hh * 32 + i], pf.x);
-                lp[i + 1] = fmaf(lp[i + 1], alpha[hh * 32 + i + 1], pf.y);
-                pk[i >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
+                const int g = 4 * kh + q;
+                *(uint4 *)(prow + ((g ^ (hrow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            uint8_t *pslot = tiles + bi * buf_bytes + rope * kChunkBytes;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *(uint4 *)(pslot + swz128(key, hh * 4 + q)) =
-                    make_uint4(pk[q * 4 + 0], pk[q * 4 + 1], pk[q * 4 + 2], pk[q * 4 + 3]);
+            lpart = fmaf(lpart, al, ps);
             fence_proxy_async();
             if (any && li > 0) {
                 // rescale the running O (needs the previous tile's O product complete);
@@ -495,18 +468,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                 } else {
                     tc_fence_after();
-                    for (int mb = 0; mb < nmb; ++mb) {
-                        uint32_t v[32];
+                    // 16 heads at a time (each step's scale factors come from shared memory)
+#pragma unroll 1
+                    for (int mq = 0; mq < 4 * nmb; ++mq) {
+                        const int hq = (mq & 3) * 16;
+                        const uint32_t ta = tO + lane_addr + (mq >> 2) * kHeads + hq;
+                        uint32_t v[16];
+                        tmem_ld16(ta, v);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const uint32_t ta = tO + lane_addr + mb * kHeads + half * 32;
-                            tmem_ld32(ta, v);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha[half * 32 + e]);
-                            tmem_st32(ta, v);
-                        }
+                        for (int e = 0; e < 16; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha[hq + e]);
+                        tmem_st16(ta, v);
                     }
                     tmem_st_wait();
                 }
@@ -521,11 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = !named_bar_or(kBarSmOr, kSoftmaxThreads, !got);
         }
         tc_fence_after();
-        half_transpose_reduce<false>(lp, lane);
-        red[warp * 64 + hh * 32 + 2 * (lane & 15)] = lp[0];
-        red[warp * 64 + hh * 32 + 2 * (lane & 15) + 1] = lp[1];
-        named_bar_sync(kBarSm, kSoftmaxThreads);
-        if (tid < kHeads) lsum[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+        const float ltot = lpart + __shfl_xor_sync(0xffffffffu, lpart, 16);
+        if (kh == 0) {
+            rn[hrow] = rmax;
+            lsum[hrow] = ltot;
+        }
         named_bar_sync(kBarSm, kSoftmaxThreads);
         const int kl = tid;  // TMEM lane = latent dim within an M-block
         const int unit_out = row * p.layers + layer;
