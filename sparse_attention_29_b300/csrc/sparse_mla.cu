@@ -256,25 +256,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c_lo = r == 0 ? 0 : nch_a, c_hi = r == 0 ? nch_a : nch;
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(kHeads, kTileKeys, false, false);
-            const uint32_t tiles_a = smem_u32(tiles), q_a = smem_u32(qs);
+            // descriptors of chunk 0; the address field (bytes >> 4) is advanced per MMA
+            const uint64_t aq0 = make_sdesc(smem_u32(qs), 16, 1024, kLayoutSW128);
+            const uint64_t bc0 = make_sdesc(smem_u32(tiles), 16, 1024, kLayoutSW128);
             bool ok = ntiles == 0 || mbar_wait(q_full, 0, KID_MLA, abort_flag);
             for (int li = 0; li < ntiles && ok; ++li) {
                 const int bi = li & 1;
                 if (li >= 2) ok = mbar_wait(&s_free[bi], ((li - 2) >> 1) & 1, KID_MLA, abort_flag);
                 if (!ok) break;
-                const uint32_t tile_a = tiles_a + (uint32_t)(bi * buf_bytes);
+                const uint64_t bct = bc0 + (uint64_t)((bi * buf_bytes) >> 4);
                 const uint32_t tSr = tS + (uint32_t)(bi * 2 * kHeads + r * kHeads);
                 for (int c = c_lo; c < c_hi && ok; ++c) {
                     ok = mbar_wait(&full[bi * 9 + c], (li >> 1) & 1, KID_MLA, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     fence_proxy_async();  // cp.async (generic proxy) data -> tensor cores
+                    const uint64_t ad = aq0 + (uint64_t)(c * (kQChunkBytes >> 4));
+                    const uint64_t bd = bct + (uint64_t)(c * (kChunkBytes >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = make_sdesc(q_a + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
-                        const uint64_t bd = make_sdesc(tile_a + c * kChunkBytes + kk * 32, 16, 1024, kLayoutSW128);
-                        mma_bf16(tSr, ad, bd, idS, (c > c_lo || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tSr, ad + 2 * kk, bd + 2 * kk, idS, (c > c_lo || kk > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
                 mma_commit(&s_full[bi]);
@@ -293,20 +294,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m_lo = r == 0 ? 0 : nmb_a, m_hi = r == 0 ? nmb_a : nmb;
         if (lane == 0) {
             const uint32_t idO = idesc_bf16(128, kHeads, true, false);
-            const uint32_t tiles_a = smem_u32(tiles);
+            // descriptors of buffer 0 (A: M-block 0, K-step 0; B: P, K-step 0); the address
+            // field (bytes >> 4) is advanced per MMA
+            const uint64_t ac0 = make_sdesc(smem_u32(tiles), kChunkBytes, 1024, kLayoutSW128);
+            const uint64_t bp0 = make_sdesc(smem_u32(tiles) + rope * kChunkBytes, 16, 1024, kLayoutSW128);
             for (int li = 0; li < ntiles; ++li) {
                 const int bi = li & 1;
                 if (!mbar_wait(&p_ready[bi], (li >> 1) & 1, KID_MLA, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t tile_a = tiles_a + (uint32_t)(bi * buf_bytes);
-                const uint32_t p_a = tile_a + rope * kChunkBytes;
+                const uint64_t boff = (uint64_t)((bi * buf_bytes) >> 4);
                 for (int j = m_lo; j < m_hi; ++j) {
+                    const uint64_t ad = ac0 + boff + (uint64_t)(j * (2 * kChunkBytes >> 4));
+                    const uint64_t bd = bp0 + boff;
 #pragma unroll
-                    for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-                        const uint64_t ad = make_sdesc(tile_a + 2 * j * kChunkBytes + ks * 2048, kChunkBytes, 1024, kLayoutSW128);
-                        const uint64_t bd = make_sdesc(p_a + ks * 32, 16, 1024, kLayoutSW128);
-                        mma_bf16(tO + j * kHeads, ad, bd, idO, (li > 0 || ks > 0) ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < kTileKeys / 16; ++ks)
+                        mma_bf16(tO + j * kHeads, ad + ks * (2048 >> 4), bd + 2 * ks, idO, (li > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&tfree[bi * 4 + j]);  // chunks 2j, 2j+1 are free again
                 }
                 mma_commit(&tfree_p[bi]);
@@ -326,20 +328,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gt = tid - kGatherWarp0 * 32;
         const uint8_t *kv_bytes = reinterpret_cast<const uint8_t *>(p.kv[layer]);
         const int64_t row_bytes = (int64_t)(p.d + p.r) * 2;
-        auto resolve_s = [&](int s) -> const uint8_t * {
+        // Row addresses are resolved ahead of use by threads gt < 64 (one key each): the
+        // token index of tile li + 2 and the page of tile li + 1 are loaded while tile li
+        // is copied, so the per-tile barrier never waits on a global load.  Same rule as
+        // resolve_row: a valid token index that does not resolve is an error.
+        const bool paged = p.layout.block_table != nullptr;
+        const int64_t seq_base = (!paged && gt < kTileKeys) ? (int64_t)__ldg(p.layout.seq_start + b) : 0;
+        auto idx_at = [&](int li) -> int {  // token index of this thread's key in tile li
+            const int j = (t_begin + li) * kTileKeys + gt;
+            return (li < ntiles && j < p.k) ? ldg_early(idx_row + j) : -1;
+        };
+        auto page_of = [&](int s) -> int {  // block-table entry of token s, or -1
+            if (!paged || s < 0) return -1;
+            const int lp = s / p.layout.page_size;
+            return lp < p.layout.pages_per_seq
+                       ? ldg_early(p.layout.block_table + (int64_t)b * p.layout.pages_per_seq + lp)
+                       : -1;
+        };
+        auto finish = [&](int s, int page) -> const uint8_t * {
             if (s < 0) return nullptr;
-            const int64_t r = resolve_row(p.layout, b, s);
-            if (r < 0) {
+            int64_t r;
+            if (paged) r = page < 0 ? -1 : (int64_t)page * p.layout.page_size + s % p.layout.page_size;
+            else r = seq_base + s;
+            if (r < 0 || r >= p.layout.num_rows) {
                 record_error(KID_MLA, ERR_BAD_INDEX);
                 return nullptr;
             }
             return kv_bytes + r * row_bytes;
         };
-        auto resolve = [&](int li, int key) -> const uint8_t * {
-            const int j = (t_begin + li) * kTileKeys + key;
-            return j < p.k ? resolve_s(__ldg(idx_row + j)) : nullptr;
-        };
-        if (gt < kTileKeys && ntiles > 0) ptrs[gt] = resolve_s(s_pre);
+        int s_nx = -1, pg_nx = -1;  // tile li + 1: token index, page
+        if (gt < kTileKeys) {
+            if (ntiles > 0) ptrs[gt] = finish(s_pre, page_of(s_pre));
+            s_nx = idx_at(1);
+        }
         named_bar_sync(kBarGa, kGatherThreads);
         // thread gt copies 16-byte granule (gt & 7) of chunk c for rows (gt >> 3) and
         // (gt >> 3) + 32, chunk by chunk, each chunk as soon as its space is free
@@ -348,6 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int bi = li & 1;
             uint8_t *buf = tiles + bi * buf_bytes;
             const uint8_t *pa = ptrs[bi * kTileKeys + ra], *pb = ptrs[bi * kTileKeys + rb];
+            int s_nn = -1;
+            if (gt < kTileKeys) {
+                pg_nx = page_of(s_nx);  // both loads complete while this tile is copied
+                s_nn = idx_at(li + 2);
+            }
             bool fail = false;
             for (int c = 0; c < nch; ++c) {
                 if (li >= 2 && !fail) {
@@ -364,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 cp_async_arrive(&full[bi * 9 + c]);
             }
-            if (gt < kTileKeys && li + 1 < ntiles) ptrs[(bi ^ 1) * kTileKeys + gt] = resolve(li + 1, gt);
+            if (gt < kTileKeys && li + 1 < ntiles) ptrs[(bi ^ 1) * kTileKeys + gt] = finish(s_nx, pg_nx);
+            s_nx = s_nn;
             if (named_bar_or(kBarGaOr, kGatherThreads, fail)) break;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
