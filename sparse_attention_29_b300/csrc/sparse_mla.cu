@@ -68,11 +68,11 @@ constexpr int kQChunkBytes = kHeads * 128;    // 64 dims x 64 heads x 2 B
 constexpr float kRescaleLog2 = 8.f;           // lazy rescale threshold (log2 units)
 constexpr int kMaxClusterSplits = 8;          // portable cluster size
 
-// named barriers: 1 softmax sync, 2 softmax OR, 3 gather sync, 4 gather OR
-constexpr int kBarSm = 1, kBarSmOr = 2, kBarGa = 3, kBarGaOr = 4;
+// named barriers: 1 softmax sync, 2 softmax OR
+constexpr int kBarSm = 1, kBarSmOr = 2;
 
 struct MlaSmem {
-    uint32_t q, tile, ptrs, rn, alpha, lsum, wts, vm, bars, total;
+    uint32_t q, tile, rn, alpha, lsum, wts, vm, bars, total;
 };
 
 __host__ __device__ inline MlaSmem mla_smem(int nch) {
@@ -82,8 +82,6 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     off += (uint32_t)nch * kQChunkBytes;
     s.tile = off;  // two tile buffers
     off += 2u * (uint32_t)nch * kChunkBytes;
-    s.ptrs = off;  // [2][64] row addresses
-    off += 2 * kTileKeys * 8;
     s.rn = off;
     off += kHeads * 4;
     s.alpha = off;
@@ -154,7 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const MlaSmem L = mla_smem(nch);
     uint8_t *qs = smem + L.q;
     uint8_t *tiles = smem + L.tile;
-    const uint8_t **ptrs = (const uint8_t **)(smem + L.ptrs);  // [2][64], null: invalid
     uint32_t *vm = (uint32_t *)(smem + L.vm);
     float *rn = (float *)(smem + L.rn);
     float *alpha = (float *)(smem + L.alpha);
@@ -194,11 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_end = min(t_begin + p.tiles_per_split, ntiles_all);
     const int ntiles = max(0, t_end - t_begin);
     const int32_t *idx_row = p.idx + (int64_t)row * p.k;
-    // the gather threads fetch tile 0's token indices now, ahead of the set-up barrier
+    // Gather warp w (0-7) copies rows 4w..4w+3 and 32+4w..32+4w+3 of every tile; its
+    // lanes 0-7 resolve those rows' addresses (lane l: row gather_row(w, l)).  They fetch
+    // tile 0's token indices now, ahead of the set-up barrier.
+    const int gw = warp - kGatherWarp0;
+    const int my_row = (lane & 7) < 4 ? 4 * gw + (lane & 7) : 32 + 4 * gw + (lane & 7) - 4;
     int s_pre = -1;
-    {
-        const int gt = tid - kGatherWarp0 * 32, j = t_begin * kTileKeys + gt;
-        if (gt >= 0 && gt < kTileKeys && ntiles > 0 && j < p.k) s_pre = __ldg(idx_row + j);
+    if (gw >= 0 && gw < kGatherThreads / 32 && lane < 8 && ntiles > 0) {
+        const int j = t_begin * kTileKeys + my_row;
+        if (j < p.k) s_pre = __ldg(idx_row + j);
     }
 
     if (tid < kHeads) {
@@ -328,15 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gt = tid - kGatherWarp0 * 32;
         const uint8_t *kv_bytes = reinterpret_cast<const uint8_t *>(p.kv[layer]);
         const int64_t row_bytes = (int64_t)(p.d + p.r) * 2;
-        // Row addresses are resolved ahead of use by threads gt < 64 (one key each): the
-        // token index of tile li + 2 and the page of tile li + 1 are loaded while tile li
-        // is copied, so the per-tile barrier never waits on a global load.  Same rule as
-        // resolve_row: a valid token index that does not resolve is an error.
+        // Each warp resolves its own rows' addresses (lanes 0-7, one row each) ahead of
+        // use: the token index of tile li + 2 and the page of tile li + 1 are loaded while
+        // tile li is copied, and the addresses reach the copying lanes by shuffles, so the
+        // warps never wait on a global load or on each other.  Same rule as resolve_row:
+        // a valid token index that does not resolve is an error.
+        const bool resolver = lane < 8;
         const bool paged = p.layout.block_table != nullptr;
-        const int64_t seq_base = (!paged && gt < kTileKeys) ? (int64_t)__ldg(p.layout.seq_start + b) : 0;
-        auto idx_at = [&](int li) -> int {  // token index of this thread's key in tile li
-            const int j = (t_begin + li) * kTileKeys + gt;
-            return (li < ntiles && j < p.k) ? ldg_early(idx_row + j) : -1;
+        const int64_t seq_base = (!paged && resolver) ? (int64_t)__ldg(p.layout.seq_start + b) : 0;
+        auto idx_at = [&](int li) -> int {  // token index of this lane's row in tile li
+            const int j = (t_begin + li) * kTileKeys + my_row;
+            return (resolver && li < ntiles && j < p.k) ? ldg_early(idx_row + j) : -1;
         };
         auto page_of = [&](int s) -> int {  // block-table entry of token s, or -1
             if (!paged || s < 0) return -1;
@@ -356,24 +359,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return kv_bytes + r * row_bytes;
         };
-        int s_nx = -1, pg_nx = -1;  // tile li + 1: token index, page
-        if (gt < kTileKeys) {
-            if (ntiles > 0) ptrs[gt] = finish(s_pre, page_of(s_pre));
-            s_nx = idx_at(1);
-        }
-        named_bar_sync(kBarGa, kGatherThreads);
+        const uint8_t *cur = resolver && ntiles > 0 ? finish(s_pre, page_of(s_pre)) : nullptr;
+        int s_nx = idx_at(1), pg_nx = -1;  // tile li + 1: token index, page
         // thread gt copies 16-byte granule (gt & 7) of chunk c for rows (gt >> 3) and
         // (gt >> 3) + 32, chunk by chunk, each chunk as soon as its space is free
         const int gi = gt & 7, ra = gt >> 3, rb = ra + 32;
         for (int li = 0; li < ntiles; ++li) {
             const int bi = li & 1;
             uint8_t *buf = tiles + bi * buf_bytes;
-            const uint8_t *pa = ptrs[bi * kTileKeys + ra], *pb = ptrs[bi * kTileKeys + rb];
-            int s_nn = -1;
-            if (gt < kTileKeys) {
-                pg_nx = page_of(s_nx);  // both loads complete while this tile is copied
-                s_nn = idx_at(li + 2);
-            }
+            const uint8_t *pa = reinterpret_cast<const uint8_t *>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(cur), lane >> 3));
+            const uint8_t *pb = reinterpret_cast<const uint8_t *>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(cur), 4 + (lane >> 3)));
+            pg_nx = page_of(s_nx);  // both loads complete while this tile is copied
+            const int s_nn = idx_at(li + 2);
             bool fail = false;
             for (int c = 0; c < nch; ++c) {
                 if (li >= 2 && !fail) {
@@ -390,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 cp_async_arrive(&full[bi * 9 + c]);
             }
-            if (gt < kTileKeys && li + 1 < ntiles) ptrs[(bi ^ 1) * kTileKeys + gt] = finish(s_nx, pg_nx);
+            cur = resolver && li + 1 < ntiles ? finish(s_nx, pg_nx) : nullptr;
             s_nx = s_nn;
-            if (named_bar_or(kBarGaOr, kGatherThreads, fail)) break;
+            if (__any_sync(0xffffffffu, fail)) break;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         asm volatile("setmaxnreg.inc.sync.aligned.u32 128;\n" ::: "memory");
