@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     griddep_launch_dependents();
-    griddep_wait();  // the index set comes from the previous kernel
+    // Everything up to griddepcontrol.wait below reads only step inputs (the work unit,
+    // the cache layout, the query), so it overlaps the end of the previous kernel.
 
     // work unit -> (row, layer, split)
     const int unit = blockIdx.x;
@@ -192,15 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntiles = max(0, t_end - t_begin);
     const int32_t *idx_row = p.idx + (int64_t)row * p.k;
     // Gather warp w (0-7) copies rows 4w..4w+3 and 32+4w..32+4w+3 of every tile; its
-    // lanes 0-7 resolve those rows' addresses (lane l: row gather_row(w, l)).  They fetch
-    // tile 0's token indices now, ahead of the set-up barrier.
+    // lanes 0-7 resolve those rows' addresses (lane l: row my_row).
     const int gw = warp - kGatherWarp0;
     const int my_row = (lane & 7) < 4 ? 4 * gw + (lane & 7) : 32 + 4 * gw + (lane & 7) - 4;
-    int s_pre = -1;
-    if (gw >= 0 && gw < kGatherThreads / 32 && lane < 8 && ntiles > 0) {
-        const int j = t_begin * kTileKeys + my_row;
-        if (j < p.k) s_pre = __ldg(idx_row + j);
-    }
+    const bool resolver = gw >= 0 && gw < kGatherThreads / 32 && lane < 8;
+    const bool paged = p.layout.block_table != nullptr;
+    const int64_t seq_base = (resolver && !paged) ? (int64_t)__ldg(p.layout.seq_start + b) : 0;
 
     if (tid < kHeads) {
         rn[tid] = -INFINITY;
@@ -231,6 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_base_sm;
+    if (warp == kQWarp && lane == 0 && ntiles > 0) {
+        // the query (a step input) streams in while the previous kernel finishes
+        const CUtensorMap *qmap = &maps.q[layer];
+        prefetch_tmap(qmap);
+        mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
+        for (int c = 0; c < nch; ++c)
+            tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
+    }
+    griddep_wait();  // the index set comes from the previous kernel
+    // the resolving gather lanes fetch tile 0's token indices first
+    int s_pre = -1;
+    if (resolver && ntiles > 0) {
+        const int j = t_begin * kTileKeys + my_row;
+        if (j < p.k) s_pre = __ldg(idx_row + j);
+    }
     const uint32_t tS = tmem;          // [2 buffers][2 issuer parts] x 64 columns
     const uint32_t tO = tmem + 256;    // nmb x 64 columns
 
@@ -241,14 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 384 x 88 = 55296 are in use.
     if (warp >= kMmaWarp) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
-      if (warp == kQWarp && lane == 0 && ntiles > 0) {
-        // ================= query TMA (then this warp issues O M-blocks) =================
-        const CUtensorMap *qmap = &maps.q[layer];
-        prefetch_tmap(qmap);
-        mbar_arrive_expect_tx(q_full, (uint32_t)(nch * kQChunkBytes));
-        for (int c = 0; c < nch; ++c)
-            tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
-      }
       if (warp == kMmaWarp || warp == kMmaWarp2) {
         // ================= S issuers =================
         // issuer r: S chunks [c_lo, c_hi) into its own S^T part
@@ -334,9 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile li is copied, and the addresses reach the copying lanes by shuffles, so the
         // warps never wait on a global load or on each other.  Same rule as resolve_row:
         // a valid token index that does not resolve is an error.
-        const bool resolver = lane < 8;
-        const bool paged = p.layout.block_table != nullptr;
-        const int64_t seq_base = (!paged && resolver) ? (int64_t)__ldg(p.layout.seq_start + b) : 0;
         auto idx_at = [&](int li) -> int {  // token index of this lane's row in tile li
             const int j = (t_begin + li) * kTileKeys + my_row;
             return (resolver && li < ntiles && j < p.k) ? ldg_early(idx_row + j) : -1;
