@@ -87,14 +87,15 @@ def load_peaks():
     return 6400.0, 1800.0, "fallback"
 
 
-def traffic_for(kernel_files, kernel):
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged."""
+def traffic_for(kernel_files, kernel, workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this
+    workload and the kernel is unchanged since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f).get(kernel)
-    if not d or d.get("source_sha") != src_sha(kernel_files):
+    if not d or d.get("source_sha") != src_sha(kernel_files) or d.get("workload_key") != workload:
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -524,7 +525,7 @@ def main():
         "kernel_ms": {"indexer": k_idx, "topk": k_topk, "sparse_mla": k_mla},
         "roofline": {"bound": "hbm", "kernel": "indexer", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": traffic_for(idx_files, "indexer"),
+                     "traffic": traffic_for(idx_files, "indexer", args.workload),
                      "algorithmic_bytes": b_idx, "peak_source": peak_src},
         "gpu_launches": launches_per_step * args.steps,
         "graph_replay": (graph_ms if isinstance(graph_ms, str) else
