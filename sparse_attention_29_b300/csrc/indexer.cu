@@ -194,6 +194,28 @@ __device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool 
     return maxpos;
 }
 
+// Packed fp32 pairs for the epilogue's weighted sum: fma.rn.f32x2 rounds each lane as
+// fmaf does, so the pairs (even, odd head) reproduce the scalar chains bit for bit.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float sum2(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+// ReLU of two accumulator words, packed
+__device__ __forceinline__ uint64_t relu2(uint32_t a, uint32_t b) {
+    return pack2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
+}
+
 // kW64: decode form (one query row of 64 padded heads per group); its weights stay in
 // registers.  Otherwise they are read from shared memory.
 template <int DI, bool kW64>
@@ -618,16 +640,15 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                     tmem_ld32(tacc, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
                     tmem_ld32(tacc + 32, *reinterpret_cast<uint32_t (*)[32]>(&v[32]));
                     tmem_ld_wait();
-                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    // four chains (heads h mod 4) as two packed pairs
+                    uint64_t a01 = 0, a23 = 0;
 #pragma unroll
                     for (int h = 0; h < 64; h += 4) {
-                        a0 = fmaf(wr[h + 0], fmaxf(__uint_as_float(v[h + 0]), 0.f), a0);
-                        a1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(v[h + 1]), 0.f), a1);
-                        a2 = fmaf(wr[h + 2], fmaxf(__uint_as_float(v[h + 2]), 0.f), a2);
-                        a3 = fmaf(wr[h + 3], fmaxf(__uint_as_float(v[h + 3]), 0.f), a3);
+                        a01 = fma2(pack2(wr[h + 0], wr[h + 1]), relu2(v[h + 0], v[h + 1]), a01);
+                        a23 = fma2(pack2(wr[h + 2], wr[h + 3]), relu2(v[h + 2], v[h + 3]), a23);
                     }
                     if (s <= pos[0])
-                        p.scores[(int64_t)r0 * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
+                        p.scores[(int64_t)r0 * p.Lmax + s] = (sum2(a01) + sum2(a23)) * ksc;
                 } else {
                     // both sets work on every tile: set e takes query rows 2e and 2e+1, and
                     // both rows' accumulators are loaded before one wait (tcgen05.wait::ld
@@ -641,16 +662,14 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                             tmem_ld32(tacc + (uint32_t)(q * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&v0[32]));
                             tmem_ld_wait();
                             const float4 *w0 = (const float4 *)(wq + q * 64);
-                            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                            uint64_t a01 = 0, a23 = 0;  // four chains as two packed pairs
 #pragma unroll
                             for (int h = 0; h < 64; h += 4) {
-                                const float4 ww = w0[h >> 2];
-                                a0 = fmaf(ww.x, fmaxf(__uint_as_float(v0[h + 0]), 0.f), a0);
-                                a1 = fmaf(ww.y, fmaxf(__uint_as_float(v0[h + 1]), 0.f), a1);
-                                a2 = fmaf(ww.z, fmaxf(__uint_as_float(v0[h + 2]), 0.f), a2);
-                                a3 = fmaf(ww.w, fmaxf(__uint_as_float(v0[h + 3]), 0.f), a3);
+                                const ulonglong2 ww = reinterpret_cast<const ulonglong2 *>(w0)[h >> 2];
+                                a01 = fma2(ww.x, relu2(v0[h + 0], v0[h + 1]), a01);
+                                a23 = fma2(ww.y, relu2(v0[h + 2], v0[h + 3]), a23);
                             }
-                            if (s <= pos[q]) p.scores[(int64_t)(r0 + q) * p.Lmax + s] = ((a0 + a1) + (a2 + a3)) * ksc;
+                            if (s <= pos[q]) p.scores[(int64_t)(r0 + q) * p.Lmax + s] = (sum2(a01) + sum2(a23)) * ksc;
                         }
                     } else {
                         // other head counts: this set's rows one at a time, 32 heads per

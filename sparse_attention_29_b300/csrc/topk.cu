@@ -425,21 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkParams p, i
         ctrl.warp_eq[warp] = w_eq;
     }
     __syncthreads();
-    if (tid == 0) {
-        uint32_t a = 0, b = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            a += ctrl.warp_st[w];
-            b += ctrl.warp_eq[w];
+    if (warp == 0) {
+        const uint32_t a = __reduce_add_sync(0xffffffffu, lane < kWarps ? ctrl.warp_st[lane] : 0u);
+        const uint32_t b = __reduce_add_sync(0xffffffffu, lane < kWarps ? ctrl.warp_eq[lane] : 0u);
+        if (lane == 0) {
+            ctrl.n_strict = a;
+            ctrl.n_eq = b;
         }
-        ctrl.n_strict = a;
-        ctrl.n_eq = b;
-        // push this slice's counts into every CTA of the cluster (itself included), so
-        // that after the barrier all reads are local and no CTA reads a peer that may
-        // already have finished
-        for (int rr = 0; rr < csize; ++rr) {
+        // push this slice's counts into every CTA of the cluster (itself included; lane
+        // rr to CTA rr), so that after the barrier all reads are local and no CTA reads a
+        // peer that may already have finished
+        if (lane < csize) {
             if (csize > 1) {
-                dsmem_st(&ctrl.peer_st[rank], (uint32_t)rr, a);
-                dsmem_st(&ctrl.peer_eq[rank], (uint32_t)rr, b);
+                dsmem_st(&ctrl.peer_st[rank], (uint32_t)lane, a);
+                dsmem_st(&ctrl.peer_eq[rank], (uint32_t)lane, b);
             } else {
                 ctrl.peer_st[0] = a;
                 ctrl.peer_eq[0] = b;
