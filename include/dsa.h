@@ -194,6 +194,32 @@ dsa_status_t dsa_sparse_mla_shared(const uint16_t *const *q_layers,
                                    uint16_t *const *out_layers, float *const *lse_layers,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Cache append, the step that feeds the path (§Lightning Indexer: the indexer keeps one
+ * key per cached token, cached like the KV cache; §MLA changes: one latent row of d + r
+ * bf16 values per token).  For each new token i of sequence seq[i] (0 <= seq[i] < B) at
+ * position pos[i], with R its physical row under `layout`:
+ *   scale      = max(max_c |k_new[i, c]|, 1e-30) / 448     (fp32)
+ *   k8[R, c]   = e4m3(k_new[i, c] / scale), round to nearest even, saturating at 448
+ *                (fp32 division)
+ *   k_scale[R] = scale
+ *   kv[R, :]   = c_new[i, :]   (when c_new is not NULL)
+ * so that the indexer then reads scale * e4m3(k8) = k_new to e4m3 precision.
+ *   k_new [n, Di] fp32, c_new [n, D] bf16 or NULL, seq / pos [n] int32;
+ *   k8_cache [num_rows, Di], k_scale [num_rows], kv_cache [num_rows, D] (NULL iff c_new is).
+ * Supported: Di in {32, 64, 128}; D % 8 == 0; k_new, k8_cache, c_new and kv_cache
+ * 16-byte aligned.  n == 0 does nothing (the arrays may then be NULL).  A token whose row
+ * does not resolve (sequence
+ * out of range, page entry missing or negative, row past num_rows) is skipped and sets
+ * the device error word.  Tokens that map to the same row race.  The kernel lets no
+ * later kernel of the stream start before it has finished (the indexer reads the key
+ * cache without waiting).
+ */
+dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *seq,
+                              const int32_t *pos, int n, int B, int Di, int D,
+                              const dsa_cache_layout_t *layout, uint8_t *k8_cache,
+                              float *k_scale, uint16_t *kv_cache, void *stream);
+
 typedef enum {
     DSA_OP_INDEXER = 0,
     DSA_OP_TOPK = 1,
@@ -211,7 +237,8 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
 /*
  * Synchronises `stream`, then reads and clears the device error word.  Returns DSA_OK
  * if no device-side check fired since the last call, else DSA_ERR_DEVICE and, if `code`
- * is not NULL, the first recorded code (kernel id << 16 | reason).
+ * is not NULL, the first recorded code (kernel id << 16 | reason; kernel ids: 1 indexer,
+ * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append).
  */
 dsa_status_t dsa_device_error(void *stream, uint32_t *code);
 

@@ -50,6 +50,11 @@ def _load():
         D = ctypes.c_double
         lib.orc_e4m3_to_double.restype = D
         lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_cache_append.restype = I
+        lib.orc_cache_append.argtypes = [P, P, P, P, I, I, I, I, P, P, I, I, ctypes.c_int64,
+                                         P, P, P]
         lib.orc_bf16_to_double.restype = D
         lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.orc_indexer_scores.restype = I
@@ -111,6 +116,36 @@ def num_threads() -> int:
 
 def e4m3_to_double(code: int) -> float:
     return _load().orc_e4m3_to_double(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    """e4m3 code of the fp32 value x (nearest, ties to even, saturating at 448)."""
+    return int(_load().orc_e4m3_encode(float(np.float32(x))))
+
+
+def cache_append(k_new, c_new, seq, pos, B, k8, k_scale, kv, seq_start=None, block_table=None,
+                 page_size=0):
+    """New tokens into copies of the caches (step 0 of the C file).  k8 [num_rows, Di] uint8,
+    k_scale [num_rows] float32 and kv [num_rows, D] uint16 are modified in place (numpy
+    arrays); returns the number of tokens whose row did not resolve."""
+    k_new = _np(k_new, np.float32)
+    n, Di = k_new.shape
+    c = None if c_new is None else _np(c_new, np.uint16)
+    D = 0 if c is None else c.shape[1]
+    seq = _np(seq, np.int32)
+    pos = _np(pos, np.int32)
+    ss = None if seq_start is None else _np(seq_start, np.int32)
+    bt = None if block_table is None else _np(block_table, np.int32)
+    pps = 0 if bt is None else bt.shape[-1]
+    for a, t in ((k8, np.uint8), (k_scale, np.float32)):
+        assert a.dtype == t and a.flags.c_contiguous
+    assert kv is None or (kv.dtype == np.uint16 and kv.flags.c_contiguous)
+    return int(_load().orc_cache_append(_ptr(k_new), None if c is None else _ptr(c), _ptr(seq),
+                                        _ptr(pos), n, B, Di, D,
+                                        None if ss is None else _ptr(ss),
+                                        None if bt is None else _ptr(bt), int(page_size),
+                                        int(pps), k8.shape[0], _ptr(k8), _ptr(k_scale),
+                                        None if kv is None else _ptr(kv)))
 
 
 def bf16_to_double(bits: int) -> float:

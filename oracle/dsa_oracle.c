@@ -43,6 +43,13 @@
  *
  * Token addressing: token s of sequence b is physical row seq_start[b] + s, or, with a
  * block table, bt[b*pages_per_seq + s/page_size]*page_size + s%page_size.
+ *
+ * 0. Cache append, the step that feeds the path [GLM53 §Lightning Indexer: the indexer
+ *    caches one key per token like the KV cache; §MLA changes: one latent row per token]:
+ *    a new token's indexer key is stored as e4m3 codes with one fp32 scale per token and
+ *    its latent row is copied.  Readings: scale = max(amax, 1e-30) / 448 and
+ *    code = e4m3(x / scale), both in fp32 (the precision the quantised codes are decided
+ *    in), rounding to nearest with ties to the even mantissa and saturating at +-448.
  */
 #include <math.h>
 #include <stdint.h>
@@ -89,6 +96,76 @@ static int64_t phys_row(int b, int s, const int32_t *seq_start, const int32_t *b
         return (int64_t)bt[(int64_t)b * pages_per_seq + s / page_size] * page_size +
                s % page_size;
     return (int64_t)seq_start[b] + s;
+}
+
+/* ---------- 0. cache append ----------------------------------------------------------- */
+
+/* e4m3 code of an fp32 value: the nearest e4m3 value, ties to the even mantissa, and
+ * magnitudes from 448 up saturating to 448 (the largest finite e4m3 value).  Below 2^-6
+ * the representable values are the multiples of 2^-9; in [2^E, 2^(E+1)) they are the
+ * multiples of 2^(E-3).  Scaling by a power of two is exact, and rint() rounds half to
+ * even in the default rounding mode. */
+uint8_t orc_e4m3_encode(float x)
+{
+    const int sign = signbit(x) ? 1 : 0;
+    const double a = fabs((double)x);
+    uint8_t code;
+    if (a >= 448.0) {
+        code = 0x7E;
+    } else if (a < ldexp(1.0, -6)) {
+        code = (uint8_t)rint(ldexp(a, 9)); /* 0..8; 8 is 2^-6, the first normal code */
+    } else {
+        int e;
+        frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+        int E = e - 1;
+        double q = rint(ldexp(a, 3 - E)); /* 8..16 */
+        if (q == 16.0) {
+            q = 8.0;
+            E += 1;
+        }
+        const int field = E + 7, mant = (int)q - 8;
+        code = (field > 15 || (field == 15 && mant == 7)) ? 0x7E : (uint8_t)((field << 3) | mant);
+    }
+    return (uint8_t)(code | (sign << 7));
+}
+
+/* Writes n new tokens into copies of the caches: token i of sequence seq[i] at position
+ * pos[i] goes to its physical row (contiguous or paged addressing as above).  A token
+ * whose row does not resolve is left out and counted; the count is returned. */
+int orc_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *seq,
+                     const int32_t *pos, int n, int B, int Di, int D,
+                     const int32_t *seq_start, const int32_t *bt, int page_size,
+                     int pages_per_seq, int64_t num_rows, uint8_t *k8, float *k_scale,
+                     uint16_t *kv)
+{
+    int skipped = 0;
+    for (int i = 0; i < n; ++i) {
+        const int b = seq[i], s = pos[i];
+        int64_t row = -1;
+        if (b >= 0 && b < B && s >= 0) {
+            if (!bt || s / page_size < pages_per_seq) {
+                if (!bt || bt[(int64_t)b * pages_per_seq + s / page_size] >= 0)
+                    row = phys_row(b, s, seq_start, bt, page_size, pages_per_seq);
+            }
+        }
+        if (row < 0 || row >= num_rows) {
+            ++skipped;
+            continue;
+        }
+        float amax = 0.0f;
+        for (int c = 0; c < Di; ++c) {
+            const float v = fabsf(k_new[(int64_t)i * Di + c]);
+            if (v > amax)
+                amax = v;
+        }
+        const float scale = (amax > 1e-30f ? amax : 1e-30f) / 448.0f;
+        for (int c = 0; c < Di; ++c)
+            k8[row * Di + c] = orc_e4m3_encode(k_new[(int64_t)i * Di + c] / scale);
+        k_scale[row] = scale;
+        if (c_new)
+            memcpy(kv + row * D, c_new + (int64_t)i * D, (size_t)D * sizeof(uint16_t));
+    }
+    return skipped;
 }
 
 /* ---------- 1. lightning indexer ---------------------------------------------------- */

@@ -16,6 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdsa.so")
 
 DSA_OK = 0
+DSA_ERR_DEVICE = 5
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_CUDA",
           4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_SCRATCH_LIMIT"}
 DSA_OP_INDEXER, DSA_OP_TOPK, DSA_OP_SPARSE_MLA = 0, 1, 2
@@ -24,7 +25,8 @@ DSA_NOALLOC_SCRATCH_BYTES = 20 << 20
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
            "dsa_sparse_mla_decode", "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_prefill",
-           "dsa_sparse_mla_shared", "dsa_workspace_bytes", "dsa_device_error")
+           "dsa_sparse_mla_shared", "dsa_cache_append", "dsa_workspace_bytes",
+           "dsa_device_error")
 
 
 class DsaError(RuntimeError):
@@ -70,6 +72,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_sparse_mla_prefill.argtypes = [P, P, LP, P, I, I, I, I, I, I, F, P, P, P, S, P]
     lib.dsa_sparse_mla_shared.restype = I
     lib.dsa_sparse_mla_shared.argtypes = [P, P, I, LP, P, I, I, I, I, I, I, F, P, P, P, S, P]
+    lib.dsa_cache_append.restype = I
+    lib.dsa_cache_append.argtypes = [P, P, P, P, I, I, I, I, LP, P, P, P, P]
     lib.dsa_workspace_bytes.restype = S
     lib.dsa_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     lib.dsa_device_error.restype = I
@@ -119,6 +123,14 @@ def dsa_indexer_scores(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, H
 def dsa_topk(scores, q_pos, rows, Lmax, k, idx, stream=None):
     st = load().dsa_topk(_ptr(scores), _ptr(q_pos), rows, Lmax, k, _ptr(idx), _stream(stream))
     _check("dsa_topk", st)
+
+
+def dsa_cache_append(k_new, c_new, seq, pos, n, B, Di, D, layout, k8_cache, k_scale, kv_cache,
+                     stream=None):
+    st = load().dsa_cache_append(_ptr(k_new), _ptr(c_new), _ptr(seq), _ptr(pos), n, B, Di, D,
+                                 ctypes.byref(layout), _ptr(k8_cache), _ptr(k_scale),
+                                 _ptr(kv_cache), _stream(stream))
+    _check("dsa_cache_append", st)
 
 
 def dsa_workspace_bytes(op, B, T, H, d, k, n_layers=1) -> int:

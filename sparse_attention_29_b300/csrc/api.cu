@@ -349,10 +349,40 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
     return mla_partial_bytes(units, splits, d);
 }
 
+dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *seq,
+                              const int32_t *pos, int n, int B, int Di, int D,
+                              const dsa_cache_layout_t *layout, uint8_t *k8_cache,
+                              float *k_scale, uint16_t *kv_cache, void *stream) {
+    if (n < 0 || B <= 0) return DSA_ERR_INVALID_ARG;
+    if (Di != 32 && Di != 64 && Di != 128) return DSA_ERR_UNSUPPORTED;
+    if (n == 0) return DSA_OK;  // nothing to append (the arrays may be NULL)
+    if (!k_new || !seq || !pos || !k8_cache || !k_scale) return DSA_ERR_INVALID_ARG;
+    if ((c_new == nullptr) != (kv_cache == nullptr)) return DSA_ERR_INVALID_ARG;
+    if (c_new && (D <= 0 || D % 8 != 0)) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(k8_cache)) return DSA_ERR_INVALID_ARG;
+    if (c_new && (!aligned16(c_new) || !aligned16(kv_cache))) return DSA_ERR_INVALID_ARG;
+    if (!layout_ok(layout, B, false)) return DSA_ERR_INVALID_ARG;
+    AppendParams p;
+    p.k_new = k_new;
+    p.c_new = c_new;
+    p.seq = seq;
+    p.pos = pos;
+    p.layout = to_layout(layout);
+    p.k8_cache = k8_cache;
+    p.k_scale = k_scale;
+    p.kv_cache = kv_cache;
+    p.n = n;
+    p.B = B;
+    p.Di = Di;
+    p.D = c_new ? D : 0;
+    return from_cuda(launch_cache_append(p, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_device_error(void *stream, uint32_t *code) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return from_cuda(cudaErrorUnknown);
-    const uint32_t words[3] = {take_error_indexer(), take_error_topk(), take_error_mla()};
+    const uint32_t words[4] = {take_error_indexer(), take_error_topk(), take_error_mla(),
+                               take_error_append()};
     uint32_t first = 0;
     for (uint32_t v : words) {
         if (v == 0xFFFFFFFFu) return DSA_ERR_CUDA;

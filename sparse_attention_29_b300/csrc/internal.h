@@ -43,6 +43,7 @@ cudaError_t set_smem_attrs(K kernel, int bytes) {
 uint32_t take_error_indexer();
 uint32_t take_error_topk();
 uint32_t take_error_mla();
+uint32_t take_error_append();
 
 // How token s of sequence b maps to a physical cache row (see dsa_cache_layout_t).
 struct CacheLayout {
@@ -106,7 +107,7 @@ struct MlaParams {
     int splits;        // key splits per (row, layer)
     int tiles_per_split;
     int cluster;       // 1: the splits of a (row, layer) form a thread-block cluster and
-                       // merge their partial results in distributed shared memory
+                       // merge their partial results through the workspace
 };
 
 // TMA descriptors of every layer: q viewed as [rows*H, d+r], kv as [num_rows, d+r] (bf16)
@@ -120,5 +121,19 @@ int mla_tile_keys();  // keys per sparse MLA tile (the split unit)
 void mla_split_plan(int rows, int k, int num_sms, int d, int *splits, int *tiles_per_split);
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
 cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);
+
+// ---- cache append: new tokens' indexer keys (quantised) and latent rows into the caches
+struct AppendParams {
+    const float *k_new;     // [n, Di] fp32
+    const uint16_t *c_new;  // [n, D] bf16, or nullptr: indexer keys only
+    const int32_t *seq;     // [n] sequence of each token
+    const int32_t *pos;     // [n] position of each token in its sequence
+    CacheLayout layout;
+    uint8_t *k8_cache;      // [num_rows, Di] e4m3 codes
+    float *k_scale;         // [num_rows]
+    uint16_t *kv_cache;     // [num_rows, D] bf16, or nullptr with c_new
+    int n, B, Di, D;
+};
+cudaError_t launch_cache_append(const AppendParams &p, cudaStream_t stream);
 
 }  // namespace dsa

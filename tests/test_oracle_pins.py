@@ -340,3 +340,95 @@ def test_decode_bytes_per_query_of_the_32k_workload():
     assert indexer == 4_333_828
     assert kv == 2_359_296
     assert oracle.indexer_flops(Hi, Di, L) == 536_870_912
+
+
+# ---- cache append (the step that feeds the path) -------------------------------------------
+
+def _finite_codes():
+    return [c for c in range(256) if c not in (0x7F, 0xFF)]
+
+
+def test_e4m3_encode_inverts_decode_on_every_code():
+    for c in _finite_codes():
+        assert oracle.e4m3_encode(oracle.e4m3_to_double(c)) == c, hex(c)
+
+
+def test_e4m3_encode_ties_go_to_even_and_neighbours_to_nearest():
+    for c in range(0, 0x7E):  # adjacent non-negative finite codes c, c + 1
+        lo, hi = oracle.e4m3_to_double(c), oracle.e4m3_to_double(c + 1)
+        mid = (lo + hi) / 2  # exact in fp32: e4m3 values carry 4 significant bits
+        assert float(np.float32(mid)) == mid
+        assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1), hex(c)
+        assert oracle.e4m3_encode(-mid) == 0x80 | (c if c % 2 == 0 else c + 1)
+        below = float(np.nextafter(np.float32(mid), np.float32(0)))
+        above = float(np.nextafter(np.float32(mid), np.float32(1e9)))
+        assert oracle.e4m3_encode(below) == c and oracle.e4m3_encode(above) == c + 1, hex(c)
+
+
+def test_e4m3_encode_saturates_at_448():
+    for x, code in ((448.0, 0x7E), (460.0, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (-1e30, 0xFE),
+                    (-449.0, 0xFE), (0.0, 0x00), (-0.0, 0x80)):
+        assert oracle.e4m3_encode(x) == code, x
+
+
+def test_e4m3_encode_matches_library_cast():
+    g = torch.Generator().manual_seed(21)
+    x = torch.cat([torch.randn(20000, generator=g) * s for s in (1e-3, 0.05, 1.0, 30.0, 300.0)])
+    ref = x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    for v, c in zip(x.tolist(), ref.tolist()):
+        assert oracle.e4m3_encode(v) == c, v
+
+
+def _append_inputs(seed, n, Di, D):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(n, Di, generator=g)
+    k[0] *= 1e-4                          # small keys: subnormal codes
+    k[1] = 0.0                            # an all-zero key: scale from the 1e-30 floor
+    c = torch.randint(-32768, 32767, (n, D), generator=g, dtype=torch.int16).view(torch.uint16)
+    return k, c
+
+
+def test_cache_append_scale_and_codes_follow_the_definition():
+    n, Di, D, B = 6, 128, 64, 2
+    k, c = _append_inputs(3, n, Di, D)
+    seq = np.array([0, 0, 1, 1, 0, 1], np.int32)
+    pos = np.array([0, 1, 0, 1, 2, 2], np.int32)
+    seq_start = np.array([0, 10], np.int32)
+    k8 = np.zeros((20, Di), np.uint8)
+    ks = np.zeros(20, np.float32)
+    kv = np.zeros((20, D), np.uint16)
+    assert oracle.cache_append(k, c, seq, pos, B, k8, ks, kv, seq_start=seq_start) == 0
+    for i in range(n):
+        r = seq_start[seq[i]] + pos[i]
+        amax = np.float32(np.abs(k[i].numpy()).max())
+        scale = np.float32(max(amax, np.float32(1e-30))) / np.float32(448)
+        assert ks[r] == scale
+        if amax > 0:  # the largest key maps to +-448 exactly
+            j = int(np.abs(k[i].numpy()).argmax())
+            assert k8[r, j] & 0x7F == 0x7E
+        dq = np.array([oracle.e4m3_to_double(int(b)) for b in k8[r]]) * float(scale)
+        step = np.abs(k[i].numpy().astype(np.float64)) * 2.0 ** -4 + 2.0 ** -9 * float(scale)
+        assert np.all(np.abs(dq - k[i].numpy()) <= step)  # within half an e4m3 step
+        assert np.array_equal(kv[r], c[i].numpy())
+    untouched = [r for r in range(20) if r not in set((seq_start[seq] + pos).tolist())]
+    assert not k8[untouched].any() and not ks[untouched].any() and not kv[untouched].any()
+
+
+def test_cache_append_paged_equals_contiguous_and_skips_bad_tokens():
+    n, Di, D, B, ps, pps = 9, 64, 16, 2, 4, 3
+    k, c = _append_inputs(4, n, Di, D)
+    seq = np.array([0, 0, 0, 0, 0, 1, 1, 1, 1], np.int32)
+    pos = np.array([0, 3, 4, 7, 11, 0, 5, 6, 12], np.int32)  # last: past the block table
+    bt = np.array([[5, 1, 3], [0, 4, 2]], np.int32)
+    num = 6 * ps
+    k8p, ksp, kvp = np.zeros((num, Di), np.uint8), np.zeros(num, np.float32), np.zeros((num, D), np.uint16)
+    assert oracle.cache_append(k, c, seq, pos, B, k8p, ksp, kvp, block_table=bt, page_size=ps) == 1
+    seq_start = np.array([0, 12], np.int32)
+    k8c, ksc, kvc = np.zeros((24, Di), np.uint8), np.zeros(24, np.float32), np.zeros((24, D), np.uint16)
+    assert oracle.cache_append(k[:8], c[:8], seq[:8], pos[:8], B, k8c, ksc, kvc, seq_start=seq_start) == 0
+    for b in range(B):
+        for s in range(12):
+            rp = bt[b, s // ps] * ps + s % ps
+            rc = seq_start[b] + s
+            assert np.array_equal(k8p[rp], k8c[rc]) and ksp[rp] == ksc[rc]
+            assert np.array_equal(kvp[rp], kvc[rc])
