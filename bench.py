@@ -316,6 +316,9 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="lean run for profiler captures: one input set, no clock pre-roll, "
                          "no per-kernel loops, graph replay, e2e or CPU baseline")
+    ap.add_argument("--append-only", action="store_true",
+                    help="only the cache-append measurement (one JSON object; for profiler "
+                         "captures of that kernel)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.warmup < 3:
@@ -336,6 +339,10 @@ def main():
     dev = torch.device("cuda", local)
     libbuild.build()
     capi.load()
+    if args.append_only:
+        hbm_peak = load_peaks()[0]
+        print(json.dumps({"cache_append": time_cache_append(dev, hbm_peak)}), flush=True)
+        return 0
 
     # baseline CPU timing first (before the GPU is busy; host cores only)
     cpu_base = None
