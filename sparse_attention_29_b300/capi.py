@@ -108,8 +108,12 @@ def version() -> str:
 
 
 def make_layout(num_rows, seq_start=None, block_table=None, page_size=0) -> CacheLayout:
+    """dsa_cache_layout_t over device tensors; the structure keeps the tensors alive, since
+    it holds only their addresses."""
     pps = 0 if block_table is None else int(block_table.shape[-1])
-    return CacheLayout(_ptr(seq_start), _ptr(block_table), int(page_size), pps, int(num_rows))
+    layout = CacheLayout(_ptr(seq_start), _ptr(block_table), int(page_size), pps, int(num_rows))
+    layout._tensors = (seq_start, block_table)
+    return layout
 
 
 def dsa_indexer_scores(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, Hi, Di, Lmax,

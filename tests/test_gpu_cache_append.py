@@ -100,7 +100,8 @@ def test_keys_only_and_empty_calls():
     skipped, st, _ = run_both(k, None, seq, pos, B, 20, Di, 0, seq_start=seq_start)
     assert skipped == 0 and st == capi.DSA_OK
     # n == 0 launches nothing and succeeds
-    layout = capi.make_layout(4, seq_start=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    ss = torch.zeros(1, dtype=torch.int32, device="cuda")  # kept alive: the layout holds its address
+    layout = capi.make_layout(4, seq_start=ss)
     k8 = torch.zeros(4, Di, dtype=torch.uint8, device="cuda")
     ks = torch.zeros(4, dtype=torch.float32, device="cuda")
     e = torch.zeros(0, dtype=torch.int32, device="cuda")
