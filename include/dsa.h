@@ -208,12 +208,11 @@ dsa_status_t dsa_sparse_mla_shared(const uint16_t *const *q_layers,
  *   k_new [n, Di] fp32, c_new [n, D] bf16 or NULL, seq / pos [n] int32;
  *   k8_cache [num_rows, Di], k_scale [num_rows], kv_cache [num_rows, D] (NULL iff c_new is).
  * Supported: Di in {32, 64, 128}; D % 8 == 0; k_new, k8_cache, c_new and kv_cache
- * 16-byte aligned.  n == 0 does nothing (the arrays may then be NULL).  A token whose row
- * does not resolve (sequence
- * out of range, page entry missing or negative, row past num_rows) is skipped and sets
- * the device error word.  Tokens that map to the same row race.  The kernel lets no
- * later kernel of the stream start before it has finished (the indexer reads the key
- * cache without waiting).
+ * 16-byte aligned.  n == 0 does nothing (the arrays may then be NULL).  A token whose
+ * row does not resolve (sequence out of range, page entry missing or negative, row past
+ * num_rows) is skipped and sets the device error word.  Tokens that map to the same row
+ * race.  The kernel lets no later kernel of the stream start before it has finished
+ * (the indexer reads the key cache without waiting).
  */
 dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *seq,
                               const int32_t *pos, int n, int B, int Di, int D,

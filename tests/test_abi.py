@@ -85,3 +85,17 @@ def test_workspace_query_without_gpu(lib):
     assert lib.dsa_workspace_bytes(0, 1, 1, 64, 512, 2048, 1) == 0
     assert lib.dsa_workspace_bytes(1, 1, 1, 64, 512, 2048, 1) == 0
     assert lib.dsa_workspace_bytes(2, 0, 1, 64, 512, 2048, 1) == ctypes.c_size_t(-1).value
+
+
+def test_layout_keeps_its_tensors_alive():
+    """The layout structure holds raw addresses, so it must keep its tensors referenced."""
+    import gc
+    import weakref
+    import torch
+    from sparse_attention_29_b300 import capi
+    t = torch.arange(4, dtype=torch.int32)
+    ref = weakref.ref(t)
+    layout = capi.make_layout(10, seq_start=t)
+    del t
+    gc.collect()
+    assert ref() is not None and layout.seq_start == ref().data_ptr()
