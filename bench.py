@@ -168,6 +168,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest of every rank's value: a job's time is that of its slowest rank.  With
+    one rank, the value itself; else an all-reduce (MAX) on the current process group."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: every rank processed `units_per_rank` in `ms` (the slowest
+    rank's time), so the job processed world x units_per_rank."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def make_workload(name, device, seed_offset=0):
     from sparse_attention_29_b300 import inputs
     return inputs.preset(name, seed=inputs.PRESETS[name]["seed"] + seed_offset, device=device)
@@ -391,11 +409,7 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    t = torch.tensor([total_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     ms_per_step = total_ms / args.steps
     layers[0].check_device_error()
 
@@ -482,7 +496,7 @@ def main():
     b_idx, b_topk, b_mla = per_query_bytes(case)
     step_bytes = b_idx + b_topk + b_mla - scores_in_step(case)
     q_tokens = case.rows
-    value = world * q_tokens / (ms_per_step * 1e-3)
+    value = job_rate(q_tokens, world, ms_per_step)
 
     # ---- e2e: host (pinned) inputs -> C-ABI calls -> host result, every step ----------
     e2e = None
@@ -554,11 +568,8 @@ def main():
         stream.wait_stream(d2h_stream)
         e2.record(stream)
         torch.cuda.synchronize()
-        t2 = torch.tensor([s2.elapsed_time(e2)], device=dev)
-        if world > 1:
-            dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t2.item()) / args.steps
-        e2e = {"value": world * q_tokens / (e2e_ms * 1e-3), "unit": UNIT,
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2), world, dev) / args.steps
+        e2e = {"value": job_rate(q_tokens, world, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "pipelined": "inputs uploaded and outputs downloaded on two copy streams "
                             "while a step computes (pinned host buffers)"}
@@ -608,7 +619,7 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "graph_replay": (graph_ms if isinstance(graph_ms, str) else
                          {"ms_per_step": graph_ms,
-                          "value": world * q_tokens / (graph_ms * 1e-3), "unit": UNIT}),
+                          "value": job_rate(q_tokens, world, graph_ms), "unit": UNIT}),
         "clocks": clocks.summary(),
     }
     if e2e:
