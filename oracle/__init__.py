@@ -58,7 +58,7 @@ def _load():
         lib.orc_bf16_to_double.restype = D
         lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.orc_indexer_scores.restype = I
-        lib.orc_indexer_scores.argtypes = [P, P, P, P, P, P, P, I, I, P, I, I, I, I, I, P]
+        lib.orc_indexer_scores.argtypes = [P, P, P, P, P, P, P, I, I, P, I, I, I, I, I, P, P]
         lib.orc_topk.restype = I
         lib.orc_topk.argtypes = [P, P, I, I, I, P]
         lib.orc_sparse_mla.restype = I
@@ -158,10 +158,11 @@ def _addressing(case):
     return seq_start, bt, int(case.page_size or 0), int(case.pages_per_seq)
 
 
-def indexer_scores(case, rows=None):
+def indexer_scores(case, with_abs=False):
     """[rows, Lmax] float64 indexer scores; -inf beyond each row's position.
 
-    rows: optional list of sequence indices to restrict to (all of a sequence's rows)."""
+    with_abs: also return the [rows, Lmax] sums of the magnitudes of every term of each
+    score, sum_h |w| * sum_c |q * k| (0 beyond the position), as (scores, abs_terms)."""
     lib = _load()
     seq_start, bt, ps, pps = _addressing(case)
     q8 = _np(case.q8, np.uint8)
@@ -171,12 +172,14 @@ def indexer_scores(case, rows=None):
     B, T = case.B, case.T
     Lmax = case.Lmax
     out = np.empty((B * T, Lmax), dtype=np.float64)
+    absum = np.empty((B * T, Lmax), dtype=np.float64) if with_abs else None
     rc = lib.orc_indexer_scores(_ptr(q8), _ptr(qs), _ptr(w), _ptr(_np(case.k8, np.uint8)),
                                 _ptr(_np(case.k_scale, np.float32)), _ptr(seq_start), _ptr(bt),
-                                ps, pps, _ptr(qp), B, T, case.Hi, case.Di, Lmax, _ptr(out))
+                                ps, pps, _ptr(qp), B, T, case.Hi, case.Di, Lmax, _ptr(out),
+                                _ptr(absum))
     if rc != 0:
         raise ValueError("oracle indexer: bad argument")
-    return out
+    return (out, absum) if with_abs else out
 
 
 def topk(scores, q_pos, k):

@@ -47,9 +47,10 @@
  * 0. Cache append, the step that feeds the path [GLM53 §Lightning Indexer: the indexer
  *    caches one key per token like the KV cache; §MLA changes: one latent row per token]:
  *    a new token's indexer key is stored as e4m3 codes with one fp32 scale per token and
- *    its latent row is copied.  Readings: scale = max(amax, 1e-30) / 448 and
- *    code = e4m3(x / scale), both in fp32 (the precision the quantised codes are decided
- *    in), rounding to nearest with ties to the even mantissa and saturating at +-448.
+ *    its latent row is copied.  Readings: the scale is an fp32 number (the per-token fp32
+ *    scale of the cache), scale = max(amax, 1e-30) / 448 evaluated in fp32; the code is
+ *    the e4m3 value nearest to the quotient x / scale itself (rounded once, ties to the
+ *    even mantissa, saturating at +-448).
  */
 #include <math.h>
 #include <stdint.h>
@@ -105,10 +106,10 @@ static int64_t phys_row(int b, int s, const int32_t *seq_start, const int32_t *b
  * the representable values are the multiples of 2^-9; in [2^E, 2^(E+1)) they are the
  * multiples of 2^(E-3).  Scaling by a power of two is exact, and rint() rounds half to
  * even in the default rounding mode. */
-uint8_t orc_e4m3_encode(float x)
+static uint8_t e4m3_encode_d(double x)
 {
     const int sign = signbit(x) ? 1 : 0;
-    const double a = fabs((double)x);
+    const double a = fabs(x);
     uint8_t code;
     if (a >= 448.0) {
         code = 0x7E;
@@ -127,6 +128,11 @@ uint8_t orc_e4m3_encode(float x)
         code = (field > 15 || (field == 15 && mant == 7)) ? 0x7E : (uint8_t)((field << 3) | mant);
     }
     return (uint8_t)(code | (sign << 7));
+}
+
+uint8_t orc_e4m3_encode(float x)
+{
+    return e4m3_encode_d((double)x);
 }
 
 /* Writes n new tokens into copies of the caches: token i of sequence seq[i] at position
@@ -159,8 +165,10 @@ int orc_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *s
                 amax = v;
         }
         const float scale = (amax > 1e-30f ? amax : 1e-30f) / 448.0f;
+        /* one rounding, of the quotient itself: the fp64 quotient of two fp32 values is
+         * never within an fp64 half-ulp of an e4m3 rounding boundary it is not equal to */
         for (int c = 0; c < Di; ++c)
-            k8[row * Di + c] = orc_e4m3_encode(k_new[(int64_t)i * Di + c] / scale);
+            k8[row * Di + c] = e4m3_encode_d((double)k_new[(int64_t)i * Di + c] / (double)scale);
         k_scale[row] = scale;
         if (c_new)
             memcpy(kv + row * D, c_new + (int64_t)i * D, (size_t)D * sizeof(uint16_t));
@@ -174,13 +182,16 @@ int orc_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *s
  * scores[t, s] = sum_h w[t,h] * ReLU( q[t,h,:] . k[s,:] )        for s = 0..q_pos[t]
  * with q = q_scale[t] * e4m3(q8), k = k_scale[row(s)] * e4m3(k8)   [GLM53 §Lightning Indexer]
  * scores[t, s] = -inf for s > q_pos[t].  Rows t = b*T + i belong to sequence b.
+ * abs_terms (may be NULL) receives sum_h |w[t,h]| * sum_c |q[t,h,c] * k[s,c]|, the sum of
+ * the magnitudes of every term of the score: what the round-off of any evaluation of the
+ * score in a shorter format is proportional to (0 past q_pos[t]).
  * Returns 0, or -1 on a bad argument.
  */
 int orc_indexer_scores(const uint8_t *q8, const float *q_scale, const float *w,
                        const uint8_t *k8, const float *k_scale,
                        const int32_t *seq_start, const int32_t *block_table, int page_size,
                        int pages_per_seq, const int32_t *q_pos, int B, int T, int Hi, int Di,
-                       int Lmax, double *scores)
+                       int Lmax, double *scores, double *abs_terms)
 {
     if (B <= 0 || T <= 0 || Hi <= 0 || Di <= 0 || Lmax <= 0)
         return -1;
@@ -201,24 +212,32 @@ int orc_indexer_scores(const uint8_t *q8, const float *q_scale, const float *w,
             for (int c = 0; c < Di; ++c)
                 q[h * Di + c] = (double)q_scale[t] *
                                 orc_e4m3_to_double(q8[((int64_t)t * Hi + h) * Di + c]);
+        double *absrow = abs_terms ? abs_terms + (int64_t)t * Lmax : NULL;
         for (int s = 0; s < Lmax; ++s) {
             if (s > p) {
                 out[s] = -INFINITY;
+                if (absrow)
+                    absrow[s] = 0.0;
                 continue;
             }
             const int64_t row = phys_row(b, s, seq_start, block_table, page_size,
                                          pages_per_seq);
             for (int c = 0; c < Di; ++c)
                 kk[c] = (double)k_scale[row] * orc_e4m3_to_double(k8[row * Di + c]);
-            double score = 0.0;
+            double score = 0.0, absum = 0.0;
             for (int h = 0; h < Hi; ++h) {
-                double logit = 0.0;
-                for (int c = 0; c < Di; ++c)
+                double logit = 0.0, alogit = 0.0;
+                for (int c = 0; c < Di; ++c) {
                     logit += q[h * Di + c] * kk[c];
+                    alogit += fabs(q[h * Di + c] * kk[c]);
+                }
                 double relu = logit > 0.0 ? logit : 0.0;
                 score += (double)w[(int64_t)t * Hi + h] * relu;
+                absum += fabs((double)w[(int64_t)t * Hi + h]) * alogit;
             }
             out[s] = score;
+            if (absrow)
+                absrow[s] = absum;
         }
         free(q);
         free(kk);

@@ -432,3 +432,30 @@ def test_cache_append_paged_equals_contiguous_and_skips_bad_tokens():
             rc = seq_start[b] + s
             assert np.array_equal(k8p[rp], k8c[rc]) and ksp[rp] == ksc[rc]
             assert np.array_equal(kvp[rp], kvc[rc])
+
+
+def test_cache_append_codes_round_the_exact_quotient_once():
+    """Every code is the e4m3 value nearest the exact rational x / scale (brute force over
+    all codes), including keys planted where a second rounding of the fp32 quotient
+    would pick the other neighbour."""
+    from fractions import Fraction
+    from planted import double_rounding_keys, nearest_e4m3_code
+    n, Di = 6, 128
+    k = np.concatenate([double_rounding_keys(n, Di, seed=3),
+                        (np.random.default_rng(4).standard_normal((2, Di)) * 3).astype(np.float32)])
+    n = k.shape[0]
+    seq = np.zeros(n, np.int32)
+    pos = np.arange(n, dtype=np.int32)
+    k8 = np.zeros((n, Di), np.uint8)
+    ks = np.zeros(n, np.float32)
+    assert oracle.cache_append(k, None, seq, pos, 1, k8, ks, None,
+                               seq_start=np.zeros(1, np.int32)) == 0
+    differs = 0
+    for i in range(n):
+        scale = Fraction(float(ks[i]))
+        for c in range(Di):
+            want = nearest_e4m3_code(Fraction(float(k[i, c])) / scale)
+            assert k8[i, c] == want, (i, c)
+            twice = oracle.e4m3_encode(np.float32(k[i, c]) / ks[i])
+            differs += int(twice != want)
+    assert differs >= 3 * 6  # the planted keys do separate the two readings
