@@ -32,7 +32,7 @@
  *     belong to sequence b.  Row t sits at position q_pos[t] and sees tokens
  *     0 .. q_pos[t] (causal; the query's own token is already cached).
  *   - The library holds no state beyond the device error word, the kernel attributes it
- *     sets once per process and the static scratch of dsa_sparse_mla_decode_noalloc;
+ *     sets once per device and the static scratch of dsa_sparse_mla_decode_noalloc;
  *     calls on different streams with different output and workspace buffers may run
  *     concurrently (dsa_sparse_mla_decode_noalloc excepted: see there).
  */
@@ -149,7 +149,9 @@ dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
  *     address up with cudaGetSymbolAddress, which may load libdsa's device code, and
  *     returns DSA_ERR_CUDA if that fails.  Make this first call before any stream
  *     capture begins.  Later calls on the device reuse the address and do nothing but
- *     check the arguments and launch.
+ *     check the arguments and launch.  The address belongs to the context it was taken
+ *     in (the device's primary context): if that context is replaced (a device reset),
+ *     the next call looks it up again, so make that call before any capture too.
  *   - Limit: a shape for which dsa_workspace_bytes(DSA_OP_SPARSE_MLA, B, 1, H, d, k, 1)
  *     exceeds DSA_NOALLOC_SCRATCH_BYTES returns DSA_ERR_SCRATCH_LIMIT before anything is
  *     launched.  The split count keeps rows x splits within the SM count, so on a
@@ -201,7 +203,7 @@ dsa_status_t dsa_sparse_mla_shared(const uint16_t *const *q_layers,
  * position pos[i], with R its physical row under `layout`:
  *   scale      = max(max_c |k_new[i, c]|, 1e-30) / 448     (fp32)
  *   k8[R, c]   = e4m3(k_new[i, c] / scale), round to nearest even, saturating at 448
- *                (fp32 division)
+ *                (the exact quotient rounded once, not an fp32 quotient rounded again)
  *   k_scale[R] = scale
  *   kv[R, :]   = c_new[i, :]   (when c_new is not NULL)
  * so that the indexer then reads scale * e4m3(k8) = k_new to e4m3 precision.

@@ -158,23 +158,51 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
 // calls on one device share it and race.
 static __device__ __align__(256) float g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-void *g_noalloc_addr[kMaxDevices];  // per device, set by the first call on that device
+// per device: the array's address and the context it was looked up in
+struct NoallocAddr {
+    CUcontext ctx;
+    void *addr;
+};
+NoallocAddr g_noalloc_addr[dsa::kMaxDevices];
 std::mutex g_noalloc_mutex;
 
-// Address of the array on the current device; the first call per device looks it up.
+PFN_cuCtxGetCurrent_v4000 get_ctx_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    });
+    return fn;
+}
+
+// Address of the array on the current device.  The first call per device looks it up;
+// the address belongs to the context it was taken in (the device's primary context), so
+// it is looked up again if that context has been replaced (after a device reset).
 dsa_status_t noalloc_scratch(void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return from_cuda(cudaErrorUnknown);
-    if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= dsa::kMaxDevices) return DSA_ERR_UNSUPPORTED;
+    PFN_cuCtxGetCurrent_v4000 ctx_current = get_ctx_current();
+    if (!ctx_current) return DSA_ERR_CUDA;
+    CUcontext ctx = nullptr;  // NULL until a runtime call has bound this thread's context
+    if (ctx_current(&ctx) != CUDA_SUCCESS) return DSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
+    NoallocAddr &a = g_noalloc_addr[dev];
+    if (!a.addr || !ctx || a.ctx != ctx) {
         void *p = nullptr;
+        // binds the device's primary context to this thread (and loads the module) if needed
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) return from_cuda(e != cudaSuccess ? e : cudaErrorUnknown);
-        g_noalloc_addr[dev] = p;
+        if (ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return DSA_ERR_CUDA;
+        a.addr = p;
+        a.ctx = ctx;
     }
-    *ptr = g_noalloc_addr[dev];
+    *ptr = a.addr;
     return DSA_OK;
 }
 

@@ -5,7 +5,7 @@
 // changes (one 576-wide latent row per token, bf16).  For every new token i of sequence
 // seq[i] at position pos[i], with physical row R(seq[i], pos[i]) of the cache layout:
 //   scale      = max(amax_c |k_new[i, c]|, 1e-30) / 448           (fp32)
-//   k8[R, c]   = e4m3_rne_satfinite(k_new[i, c] / scale)          (fp32 division)
+//   k8[R, c]   = e4m3_rne_satfinite(k_new[i, c] / scale)          (the quotient rounded once)
 //   k_scale[R] = scale
 //   kv[R, :]   = c_new[i, :]                                       (bf16 copy)
 // so that scale * e4m3(k8[R, c]) is k_new[i, c] to e4m3 precision, the form the indexer
@@ -15,7 +15,13 @@
 // a lane holds Di/32 consecutive key values (one vector load), the warp reduces their
 // maximum by shuffles, each lane converts its values with the hardware e4m3 conversion
 // (cvt.rn.satfinite.e4m3x2.f32: round to nearest even, saturating) and stores its codes
-// as one word; the latent row moves as 16-byte loads and stores.
+// as one word; the latent row moves as 16-byte loads and stores.  The code is the e4m3
+// rounding of the exact quotient: the fp32 quotient is taken rounded toward zero and,
+// when inexact (a non-zero fma remainder), its last bit is set ("round to odd"); an
+// fp32 value rounded to odd carries enough bits (24 >= 4 + 2) for its rounding to the
+// 4-bit e4m3 significand to equal the rounding of the exact quotient (Boldo and
+// Melquiond, "Emulation of FMA and correctly rounded sums: proved algorithms using
+// rounding to odd", IEEE Trans. Computers 2008).
 //
 // The kernel waits for its predecessor before touching memory and does not let its own
 // successor start early: the indexer reads the key cache without waiting (it treats its
@@ -36,6 +42,14 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// x / s rounded to odd in fp32: the quotient rounded toward zero, with its last bit set
+// when it is inexact (x - q s != 0; the fma gives that remainder's sign exactly).
+__device__ __forceinline__ float div_round_odd(float x, float s) {
+    const float q = __fdiv_rz(x, s);
+    const float r = fmaf(-q, s, x);
+    return r != 0.f ? __int_as_float(__float_as_int(q) | 1) : q;
 }
 
 template <int DI>
@@ -91,14 +105,15 @@ __global__ void __launch_bounds__(32 * kTokensPerBlock) cache_append_kernel(cons
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float scale = fmaxf(amax, 1e-30f) / kE4m3Max;
     uint8_t *dst = p.k8_cache + row * DI + kPer * lane;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) x[e] = div_round_odd(x[e], scale);
     if constexpr (kPer == 4) {
-        const uint32_t c = (uint32_t)e4m3x2(x[0] / scale, x[1] / scale) |
-                           ((uint32_t)e4m3x2(x[2] / scale, x[3] / scale) << 16);
+        const uint32_t c = (uint32_t)e4m3x2(x[0], x[1]) | ((uint32_t)e4m3x2(x[2], x[3]) << 16);
         *reinterpret_cast<uint32_t *>(dst) = c;
     } else if constexpr (kPer == 2) {
-        *reinterpret_cast<uint16_t *>(dst) = e4m3x2(x[0] / scale, x[1] / scale);
+        *reinterpret_cast<uint16_t *>(dst) = e4m3x2(x[0], x[1]);
     } else {
-        *dst = (uint8_t)(e4m3x2(x[0] / scale, 0.f) & 0xFFu);
+        *dst = (uint8_t)(e4m3x2(x[0], 0.f) & 0xFFu);
     }
     if (lane == 0) p.k_scale[row] = scale;
 

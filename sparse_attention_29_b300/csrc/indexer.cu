@@ -728,12 +728,9 @@ cudaError_t launch_di(const IndexerParams &p, const CUtensorMap &kmap,
                       cudaStream_t stream) {
     const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc);
     const size_t bytes = L.total + 1024;
-    static int attr_set_bytes = 0;  // per process; max over calls
-    if ((int)bytes > attr_set_bytes) {
-        cudaError_t e = set_smem_attrs(indexer_kernel<DI, kW64>, (int)bytes);
-        if (e != cudaSuccess) return e;
-        attr_set_bytes = (int)bytes;
-    }
+    static AttrCache attrs;
+    cudaError_t e = ensure_smem_attrs(attrs, indexer_kernel<DI, kW64>, (int)bytes);
+    if (e != cudaSuccess) return e;
     return launch_pdl(indexer_kernel<DI, kW64>, dim3(grid), dim3(EpiCfg<kW64>::kThreads), bytes, stream, kmap,
                       kmap128, qmap, p);
 }

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <utility>
 
 #include "dsa.h"
@@ -30,12 +31,35 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Kernel attributes set once per kernel: dynamic shared memory limit and carveout.
+// Kernel attributes: dynamic shared memory limit and carveout.
 template <typename K>
 cudaError_t set_smem_attrs(K kernel, int bytes) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
+// Function attributes belong to a device, so what a kernel has been given is remembered
+// per device (the largest request so far); the mutex makes concurrent first calls from
+// several host threads safe.  One AttrCache per kernel (instantiation).
+constexpr int kMaxDevices = 64;
+struct AttrCache {
+    std::mutex mu;
+    int bytes[kMaxDevices] = {};
+};
+
+template <typename K>
+cudaError_t ensure_smem_attrs(AttrCache &cache, K kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(cache.mu);
+    if (cache.bytes[dev] >= bytes) return cudaSuccess;
+    e = set_smem_attrs(kernel, bytes);
+    if (e != cudaSuccess) return e;
+    cache.bytes[dev] = bytes;
+    return cudaSuccess;
 }
 
 // Read and clear the device error word of each kernel file (0: no error;

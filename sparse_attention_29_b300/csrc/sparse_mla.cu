@@ -30,11 +30,17 @@
 // Softmax: the M = 64 accumulator puts head 16w + i in TMEM lane 32w + i (w = warp,
 // i < 16); a 16x32bx2 tcgen05.ld hands thread i < 16 of warp w keys 0-31 of that head
 // and thread 16 + i keys 32-63, so all 128 softmax threads work and a head's maximum
-// and sum over the tile are one thread's plus one shuffle.  The probabilities are
-// written (bf16, one 128-byte row of 64 keys per head) over the tile's rope chunk,
-// which S no longer needs.  Online softmax rescales O in tensor memory only when
-// a head's running maximum grows by more than 2^8 (the result is the same; the
-// unnormalised terms just stay < 2^8).
+// and sum over the tile are one thread's plus one shuffle.  A probability is
+// p = 2^((S - m) * scale * log2 e) with S and the running maximum m in raw logit units,
+// so the one rounded product sees the small difference, not the large logits.  Each p
+// goes to the value product as two bf16 halves, hi = bf16(p) and lo = bf16(p - hi):
+// the two MMAs over the same latent chunk (hi, then lo) weigh every value row with
+// hi + lo, which is p to a relative 2^-16 instead of bf16's 2^-8, and the running sum
+// adds exactly hi + lo.  hi is written (one 128-byte row of 64 keys per head) over the
+// tile's rope chunk, which S no longer needs; lo goes to one separate buffer, reused
+// once the previous tile's value product is done.  Online softmax rescales O in tensor
+// memory only when a head's running maximum grows by more than 2^8 (the result is the
+// same; the unnormalised terms just stay < 2^8).
 //
 // Rows with few keys are split over several CTAs (split-KV), merged with the log-sum-exp
 // rule.  Up to kMaxClusterSplits splits of a row run as one thread-block cluster: each CTA
@@ -67,12 +73,13 @@ constexpr int kChunkBytes = kTileKeys * 128;  // 64 dims x 64 keys x 2 B
 constexpr int kQChunkBytes = kHeads * 128;    // 64 dims x 64 heads x 2 B
 constexpr float kRescaleLog2 = 8.f;           // lazy rescale threshold (log2 units)
 constexpr int kMaxClusterSplits = 8;          // portable cluster size
+static_assert(kMaxClusterSplits * kHeads * 4 <= kChunkBytes, "merge weights alias P_lo");
 
 // named barriers: 1 softmax sync, 2 softmax OR
 constexpr int kBarSm = 1, kBarSmOr = 2;
 
 struct MlaSmem {
-    uint32_t q, tile, rn, alpha, lsum, wts, vm, bars, total;
+    uint32_t q, tile, plo, rn, alpha, lsum, wts, vm, bars, total;
 };
 
 __host__ __device__ inline MlaSmem mla_smem(int nch) {
@@ -82,14 +89,15 @@ __host__ __device__ inline MlaSmem mla_smem(int nch) {
     off += (uint32_t)nch * kQChunkBytes;
     s.tile = off;  // two tile buffers
     off += 2u * (uint32_t)nch * kChunkBytes;
+    s.plo = off;   // low halves of a tile's probabilities (one buffer, 1024-aligned)
+    s.wts = off;   // cluster merge, after the last tile: [split][head] weights
+    off += kChunkBytes;
     s.rn = off;
     off += kHeads * 4;
     s.alpha = off;
     off += kHeads * 4;
     s.lsum = off;
     off += kHeads * 4;
-    s.wts = off;  // cluster merge: [split][head] weights
-    off += kMaxClusterSplits * kHeads * 4;
     s.vm = off;  // [2 buffers][2] key-validity words of a tile
     off += 16;
     s.bars = off;
@@ -152,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const MlaSmem L = mla_smem(nch);
     uint8_t *qs = smem + L.q;
     uint8_t *tiles = smem + L.tile;
+    uint8_t *plo = smem + L.plo;
     uint32_t *vm = (uint32_t *)(smem + L.vm);
     float *rn = (float *)(smem + L.rn);
     float *alpha = (float *)(smem + L.alpha);
@@ -304,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // field (bytes >> 4) is advanced per MMA
             const uint64_t ac0 = make_sdesc(smem_u32(tiles), kChunkBytes, 1024, kLayoutSW128);
             const uint64_t bp0 = make_sdesc(smem_u32(tiles) + rope * kChunkBytes, 16, 1024, kLayoutSW128);
+            const uint64_t bl0 = make_sdesc(smem_u32(plo), 16, 1024, kLayoutSW128);
             for (int li = 0; li < ntiles; ++li) {
                 const int bi = li & 1;
                 if (!mbar_wait(&p_ready[bi], (li >> 1) & 1, KID_MLA, abort_flag)) break;
@@ -312,9 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = m_lo; j < m_hi; ++j) {
                     const uint64_t ad = ac0 + boff + (uint64_t)(j * (2 * kChunkBytes >> 4));
                     const uint64_t bd = bp0 + boff;
+                    // the same latent chunk pair weighed by the high, then the low halves
 #pragma unroll
                     for (int ks = 0; ks < kTileKeys / 16; ++ks)
                         mma_bf16(tO + j * kHeads, ad + ks * (2048 >> 4), bd + 2 * ks, idO, (li > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int ks = 0; ks < kTileKeys / 16; ++ks)
+                        mma_bf16(tO + j * kHeads, ad + ks * (2048 >> 4), bl0 + 2 * ks, idO, 1u);
                     mma_commit(&tfree[bi * 4 + j]);  // chunks 2j, 2j+1 are free again
                 }
                 mma_commit(&tfree_p[bi]);
@@ -406,8 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hrow = warp * 16 + (lane & 15);
         const int kh = lane >> 4;
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        float rmax = -INFINITY;  // running maximum of this head (log2 units)
-        float lpart = 0.f;       // running sum of this thread's probabilities
+        const float c = p.scale_log2;  // softmax scale * log2 e
+        float rmax = -INFINITY;  // running maximum of this head's raw logits q.c
+        float lpart = 0.f;       // running sum of this thread's probabilities (hi + lo)
         // validity of key `key` of tile li (same rule as the gathers)
         auto key_valid = [&](int li, int key) -> bool {
             const int j = (t_begin + li) * kTileKeys + key;
@@ -447,13 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                x[e] = ((vmask >> e) & 1u) ? x[e] * p.scale_log2 : -INFINITY;
+                x[e] = ((vmask >> e) & 1u) ? x[e] : -INFINITY;
                 m = fmaxf(m, x[e]);
             }
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-            const bool need = m > rmax + kRescaleLog2;
+            // (m - rmax) * c is +inf while nothing was valid yet, NaN (false) if still nothing is
+            const bool need = (m - rmax) * c > kRescaleLog2;
             const float rnew = need ? m : rmax;
-            const float al = need ? ex2_approx(rmax - rnew) : 1.f;
+            const float al = need ? ex2_approx((rmax - rnew) * c) : 1.f;
             rmax = rnew;
             if (kh == 0) alpha[hrow] = al;
             if (warp == 0) {
@@ -464,53 +480,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                     vm[2 * (bi ^ 1) + 1] = m1;
                 }
             }
+            // the low halves' buffer and the running O are the previous tile's value
+            // product's until it is complete
+            bool got_o = true;
+            if (li > 0) got_o = mbar_wait(o_done, (li - 1) & 1, KID_MLA, abort_flag);
             const bool any = named_bar_or(kBarSmOr, kSoftmaxThreads, need);
-            // probabilities of this head for its 32 keys; the sum takes the rounded values.
-            // P^T goes over the tile's rope chunk, K-major: head h's 64 keys in one
-            // 128-byte row (128-byte swizzle), keys 8g..8g+7 in 16-byte granule g.
+            if (named_bar_or(kBarSmOr, kSoftmaxThreads, !got_o)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // probabilities of this head for its 32 keys, as hi + lo bf16 pairs; the sum
+            // takes hi + lo (exact in fp32).  P^T goes K-major, head h's 64 keys in one
+            // 128-byte row (128-byte swizzle), keys 8g..8g+7 in 16-byte granule g: hi over
+            // the tile's rope chunk, lo into the low-halves buffer.
             uint8_t *prow = tiles + bi * buf_bytes + rope * kChunkBytes + hrow * 128;
+            uint8_t *lrow = plo + hrow * 128;
             float ps = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t pk[4];
+                uint32_t pk[4], lk[4];
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                     const int i = 8 * q + e;
-                    const float p0 = rmax != -INFINITY ? ex2_approx(x[i] - rmax) : 0.f;
-                    const float p1 = rmax != -INFINITY ? ex2_approx(x[i + 1] - rmax) : 0.f;
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                    const float2 pf = __bfloat1622float2(pb);
-                    ps += pf.x + pf.y;
-                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
+                    const float p0 = rmax != -INFINITY ? ex2_approx((x[i] - rmax) * c) : 0.f;
+                    const float p1 = rmax != -INFINITY ? ex2_approx((x[i + 1] - rmax) * c) : 0.f;
+                    const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
+                    const float2 hf = __bfloat1622float2(hb);
+                    const __nv_bfloat162 lb = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                    const float2 lf = __bfloat1622float2(lb);
+                    ps += (hf.x + lf.x) + (hf.y + lf.y);
+                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hb);
+                    lk[e >> 1] = *reinterpret_cast<const uint32_t *>(&lb);
                 }
                 const int g = 4 * kh + q;
                 *(uint4 *)(prow + ((g ^ (hrow & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *(uint4 *)(lrow + ((g ^ (hrow & 7)) << 4)) = make_uint4(lk[0], lk[1], lk[2], lk[3]);
             }
             lpart = fmaf(lpart, al, ps);
             fence_proxy_async();
             if (any && li > 0) {
-                // rescale the running O (needs the previous tile's O product complete);
-                // here thread = TMEM lane = latent dim within each M-block
-                const bool got_o = mbar_wait(o_done, (li - 1) & 1, KID_MLA, abort_flag);
-                if (named_bar_or(kBarSmOr, kSoftmaxThreads, !got_o)) {
-                    ok = false;
-                } else {
-                    tc_fence_after();
-                    // 16 heads at a time (each step's scale factors come from shared memory)
+                // rescale the running O (the previous tile's O product is complete, above);
+                // here thread = TMEM lane = latent dim within each M-block; 16 heads at a
+                // time (each step's scale factors come from shared memory)
 #pragma unroll 1
-                    for (int mq = 0; mq < 4 * nmb; ++mq) {
-                        const int hq = (mq & 3) * 16;
-                        const uint32_t ta = tO + lane_addr + (mq >> 2) * kHeads + hq;
-                        uint32_t v[16];
-                        tmem_ld16(ta, v);
-                        tmem_ld_wait();
+                for (int mq = 0; mq < 4 * nmb; ++mq) {
+                    const int hq = (mq & 3) * 16;
+                    const uint32_t ta = tO + lane_addr + (mq >> 2) * kHeads + hq;
+                    uint32_t v[16];
+                    tmem_ld16(ta, v);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha[hq + e]);
-                        tmem_st16(ta, v);
-                    }
-                    tmem_st_wait();
+                    for (int e = 0; e < 16; ++e)
+                        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha[hq + e]);
+                    tmem_st16(ta, v);
                 }
+                tmem_st_wait();
             }
             tc_fence_before();
             mbar_arrive(&p_ready[bi]);
@@ -565,10 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kl < p.H && p.lse[layer]) {
                 const float l = lsum[kl];
                 p.lse[layer][(int64_t)row * p.H + kl] =
-                    l > 0.f ? (rn[kl] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    l > 0.f ? (rn[kl] * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
         } else {
-            // unnormalised partial: O [64][d], then R [64] (log2 domain), l [64]
+            // unnormalised partial: O [64][d], then R [64] (raw logit units), l [64]
             float *part = p.partial + ((int64_t)unit_out * p.splits + split) * (size_t)(kHeads * p.d + 2 * kHeads);
             for (int mb = 0; mb < nmb; ++mb) {
                 const int dim = mb * 128 + kl;
@@ -645,13 +670,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rs[s] = s < p.splits ? __uint_as_float(dsmem_ld(&rn[h], (uint32_t)s)) : -INFINITY;
                 ls[s] = s < p.splits ? __uint_as_float(dsmem_ld(&lsum[h], (uint32_t)s)) : 0.f;
             }
-            float R = -INFINITY;
+            float R = -INFINITY;  // raw logit units, like every split's maximum
 #pragma unroll
             for (int s = 0; s < kMaxClusterSplits; ++s) R = fmaxf(R, rs[s]);
             float Lsum = 0.f;
 #pragma unroll
             for (int s = 0; s < kMaxClusterSplits; ++s) {
-                rs[s] = (R == -INFINITY || rs[s] == -INFINITY) ? 0.f : ex2_approx(rs[s] - R);
+                rs[s] = (R == -INFINITY || rs[s] == -INFINITY) ? 0.f : ex2_approx((rs[s] - R) * p.scale_log2);
                 Lsum = fmaf(rs[s], ls[s], Lsum);
             }
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
@@ -659,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kMaxClusterSplits; ++s) wts[s * kHeads + h] = rs[s] * inv;
             if (split == 0 && h < p.H && p.lse[layer])
                 p.lse[layer][(int64_t)row * p.H + h] =
-                    Lsum > 0.f ? (R + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+                    Lsum > 0.f ? (R * p.scale_log2 + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         }
         __syncthreads();
         const int ds = ((p.d + p.splits - 1) / p.splits + 3) & ~3;
@@ -728,8 +753,8 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const MlaP
         rmax = fmaxf(rmax, rs[s]);
     }
     float ltot = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        ws[s] = (rmax == -INFINITY || rs[s] == -INFINITY) ? 0.f : ex2_approx(rs[s] - rmax);
+    for (int s = 0; s < p.splits; ++s) {  // maxima in raw logit units
+        ws[s] = (rmax == -INFINITY || rs[s] == -INFINITY) ? 0.f : ex2_approx((rs[s] - rmax) * p.scale_log2);
         ltot = fmaf(ws[s], __ldg(part + s * stride + kHeads * p.d + kHeads + h), ltot);
     }
     const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
@@ -752,7 +777,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const MlaP
     }
     if (threadIdx.x == 0 && p.lse[layer])
         p.lse[layer][(int64_t)row * p.H + h] =
-            ltot > 0.f ? (rmax + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+            ltot > 0.f ? (rmax * p.scale_log2 + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace
@@ -834,13 +859,9 @@ cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStrea
     const int nch = p.d / 64 + 1;
     const MlaSmem L = mla_smem(nch);
     const size_t bytes = L.total + 1024;
-    static int attr_bytes = 0;
-    if ((int)bytes > attr_bytes) {
-        const int max_bytes = (int)(mla_smem(9).total + 1024);  // every width fits
-        cudaError_t e = set_smem_attrs(sparse_mla_kernel, max_bytes);
-        if (e != cudaSuccess) return e;
-        attr_bytes = max_bytes;
-    }
+    static AttrCache attrs;  // set to the largest width's need: every width fits
+    cudaError_t ea = ensure_smem_attrs(attrs, sparse_mla_kernel, (int)(mla_smem(9).total + 1024));
+    if (ea != cudaSuccess) return ea;
     const int units = p.B * p.T * p.layers;
     if (units <= 0) return cudaSuccess;
     MlaParams q = p;

@@ -595,12 +595,9 @@ cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream) {
     topk_shape(p, num_sms, csize, slice_cap);
     const size_t bytes = topk_layout(slice_cap).total;
     if (bytes > 227 * 1024) return cudaErrorInvalidValue;
-    static int attr_bytes = 0;
-    if ((int)bytes > attr_bytes) {
-        cudaError_t e = set_smem_attrs(topk_kernel, 227 * 1024);  // every slice size fits
-        if (e != cudaSuccess) return e;
-        attr_bytes = 227 * 1024;
-    }
+    static AttrCache attrs;  // every slice size fits
+    cudaError_t ea = ensure_smem_attrs(attrs, topk_kernel, 227 * 1024);
+    if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.rows * csize);
     cfg.blockDim = dim3(kThreads);
