@@ -1,17 +1,23 @@
 """Shared comparison rules for the GPU-vs-oracle parity tests.
 
 Tolerances (restating the acceptance bars, with the readings taken where they are open):
-  * integer-valued workload: indexer scores and top-k indices bit-exact;
-  * indexer scores elsewhere: |gpu - ref| <= 1e-3 * max(|ref|, 1e-2 * rms(row)).  The floor
-    reads "1e-3 relative" for scores near zero, where a relative error is undefined; it
-    still sits an order of magnitude above the fp32 round-off of the kernel's sums;
+  * integer-valued workloads: indexer scores and top-k indices bit-exact;
+  * indexer scores elsewhere: |gpu - ref| <= 1e-3 * max(|ref|, 1e-3 * rms(row)), the
+    "1e-3 relative" bar with a floor for scores near zero -- except where the score is
+    a near-cancellation of large terms, where no fp32 evaluation can meet a relative bar:
+    there the bar is the textbook round-off bound of the fp32 sums themselves,
+    (Di + Hi + 2) * 2^-23 * A, with A = sum_h |w_h| sum_c |q_hc k_c| (the oracle's
+    `abs_terms`; Higham, Accuracy and Stability of Numerical Algorithms, eq. 3.5, with
+    the unit 2^-23 so that truncating accumulation is covered too);
   * top-k sets equal, except tokens whose oracle score lies within 1e-3 relative of the
     oracle's k-th score;
   * attention outputs, against the oracle fed the GPU's own index set: max-abs <= 1e-2 and
-    relative Frobenius error <= 5e-3; lse within 2.5e-3 (probabilities enter the second
-    product as bf16, a relative error of at most 2^-9 on their sum);
-  * integer-valued workload outputs: |gpu - ref| <= 0.5 ulp_bf16(ref) + 2^-8 * max_j
-    |v_j - ref| (bf16 probabilities perturb the convex weights by at most 2^-9 each).
+    relative Frobenius error <= 5e-3; lse within 2.5e-3;
+  * integer-valued workload outputs: within one bf16 ulp of the correctly rounded oracle
+    value, plus the fp32 error of forming the weighted mean before that rounding,
+    (2^-14 + 2 n 2^-23) * max_j |v_j| for n selected keys (softmax weights to a relative
+    2^-16 from the hi/lo bf16 split, 2^-21 from the exponential, and fp32 accumulation
+    of 2n products); lse within fp32 round-off, 2^-16 + 2^-20 |lse|.
 """
 import numpy as np
 import torch
@@ -20,7 +26,8 @@ import oracle
 from sparse_attention_29_b300 import inputs
 
 SCORE_RTOL = 1e-3
-SCORE_FLOOR = 1e-2
+SCORE_FLOOR = 1e-3
+FP32_UNIT = 2.0 ** -23
 TOPK_RTOL = 1e-3
 OUT_MAX_ABS = 1e-2
 OUT_REL_FRO = 5e-3
@@ -36,15 +43,19 @@ def visible_mask(q_pos, Lmax):
     return s <= np.asarray(q_pos)[:, None]
 
 
-def check_scores(gpu_scores, ref, q_pos):
+def check_scores(gpu_scores, ref, q_pos, abs_terms=None, Hi=64, Di=128):
+    """`ref` and `abs_terms` from oracle.indexer_scores(case, with_abs=True)."""
     g = cpu(gpu_scores).double().numpy()
     vis = visible_mask(cpu(q_pos).numpy(), ref.shape[1])
     worst = 0.0
+    gamma = (Di + Hi + 2) * FP32_UNIT
     for t in range(ref.shape[0]):
         m = vis[t]
         r, x = ref[t, m], g[t, m]
         rms = np.sqrt(np.mean(r * r)) if r.size else 0.0
         tol = SCORE_RTOL * np.maximum(np.abs(r), SCORE_FLOOR * rms)
+        if abs_terms is not None:
+            tol = np.maximum(tol, gamma * abs_terms[t, m])
         err = np.abs(x - r)
         bad = np.nonzero(err > tol)[0]
         assert bad.size == 0, (f"row {t}: {bad.size} scores off, first at s={bad[0]}: "
@@ -52,6 +63,13 @@ def check_scores(gpu_scores, ref, q_pos):
         if r.size:
             worst = max(worst, float(np.max(err / np.maximum(tol, 1e-300))))
     return worst
+
+
+def check_case_scores(gpu_scores, case):
+    """GPU scores of every row of `case` against the oracle; returns the oracle scores."""
+    ref, absum = oracle.indexer_scores(case, with_abs=True)
+    check_scores(gpu_scores, ref, case.q_pos, absum, Hi=case.Hi, Di=case.Di)
+    return ref
 
 
 def check_topk_sets(gpu_idx, ref_scores, q_pos, k):
@@ -101,18 +119,29 @@ def check_mla(gpu_out, gpu_lse, ref_out, ref_lse):
     return max_abs, fro
 
 
+def bf16_round(x):
+    """Round float64 values to the nearest bf16 value (8 significant bits, ties to even),
+    directly from float64 (no intermediate fp32 rounding)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                      # x = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
 def bf16_ulp(x):
-    a = np.abs(x)
-    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
-    return 2.0 ** (e - 7)
+    """Spacing of bf16 values at |x| (2^(E-7) for |x| in [2^E, 2^(E+1)))."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(np.maximum(a, 2.0 ** -126))
+    return np.ldexp(1.0, e - 8)
 
 
-def check_mla_integer(gpu_out, case, idx, ref_out, layer=0):
-    """Bound from the arithmetic for exactly representable inputs (see module doc)."""
+def check_mla_integer(gpu_out, gpu_lse, case, idx, ref_out, ref_lse, layer=0):
+    """Outputs within one bf16 ulp of the correctly rounded oracle value plus the bound on
+    forming the weighted mean in fp32 (module doc); lse within fp32 round-off."""
     g = cpu(gpu_out).double().numpy()
     kv = cpu(case.kv[layer]).double().numpy()
     ix = cpu(idx).numpy()
     rows, H, d = ref_out.shape
+    worst_ulps = 0.0
     for t in range(rows):
         b = t // case.T
         sel = ix[t][ix[t] >= 0]
@@ -121,13 +150,19 @@ def check_mla_integer(gpu_out, case, idx, ref_out, layer=0):
         else:
             bt = cpu(case.block_table).numpy()
             phys = bt[b, sel // case.page_size] * case.page_size + sel % case.page_size
-        V = kv[phys, :d]                                    # [n, d]
-        for h in range(H):
-            o = ref_out[t, h]
-            spread = np.max(np.abs(V - o[None, :]), axis=0)
-            tol = 0.5 * bf16_ulp(o) + 2.0 ** -8 * spread + 1e-12
-            err = np.abs(g[t, h] - o)
-            assert np.all(err <= tol), (t, h, float(np.max(err - tol)))
+        vmax = float(np.abs(kv[phys, :d]).max()) if sel.size else 0.0
+        pre = (2.0 ** -14 + 2 * sel.size * FP32_UNIT) * vmax
+        rn = bf16_round(ref_out[t])                         # [H, d]
+        err = np.abs(g[t] - rn)
+        tol = bf16_ulp(rn) + pre
+        assert np.all(err <= tol), (t, float(np.max(err - tol)))
+        worst_ulps = max(worst_ulps, float(np.max(err / bf16_ulp(rn))))
+    gl = cpu(gpu_lse).double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(gl), fin)
+    dl = np.abs(gl[fin] - ref_lse[fin])
+    assert np.all(dl <= 2.0 ** -16 + 2.0 ** -20 * np.abs(ref_lse[fin])), float(dl.max())
+    return worst_ulps
 
 
 def subcase(case, seqs=None, rows_in_seq=None):

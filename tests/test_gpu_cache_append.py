@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_scores
+from parity import check_case_scores
 from sparse_attention_29_b300 import build, capi
 
 pytestmark = pytest.mark.gpu
@@ -147,4 +147,18 @@ def test_appended_keys_score_like_the_definition():
     sub.k8, sub.k_scale = torch.from_numpy(k8_ref), torch.from_numpy(ks_ref)
     sub.seq_start, sub.block_table, sub.page_size, sub.pages_per_seq = torch.from_numpy(seq_start), None, 0, 0
     sub.B, sub.T, sub.Hi, sub.Di, sub.Lmax, sub.lengths = B, 1, Hi, Di, L, [L]
-    check_scores(scores, oracle.indexer_scores(sub), q_pos)
+    check_case_scores(scores, sub)
+
+
+
+def test_codes_round_the_exact_quotient_once():
+    """Keys planted so that the fp32 quotient x / scale sits exactly on an e4m3 midpoint
+    while the exact quotient lies on the other neighbour's side: the codes must be those
+    of the exact quotient rounded once (the oracle's reading), bit for bit."""
+    from planted import double_rounding_keys
+    Di, n = 128, 8
+    k = torch.from_numpy(double_rounding_keys(n, Di, seed=21))
+    seq = np.zeros(n, np.int32)
+    pos = np.arange(n, dtype=np.int32)
+    skipped, st, _ = run_both(k, None, seq, pos, 1, n, Di, 0, seq_start=np.zeros(1, np.int32))
+    assert skipped == 0 and st == capi.DSA_OK

@@ -70,8 +70,8 @@ def run_and_check(name, seqs, rows_in_seq):
     lay.check_device_error()
     sub, rows = compact(case, seqs, rows_in_seq)
     ri = torch.tensor(rows, device="cuda")
-    ref_scores = oracle.indexer_scores(sub)
-    check_scores(lay.scores[ri, :sub.Lmax], ref_scores, sub.q_pos)
+    ref_scores, abs_terms = oracle.indexer_scores(sub, with_abs=True)
+    check_scores(lay.scores[ri, :sub.Lmax], ref_scores, sub.q_pos, abs_terms, Hi=sub.Hi, Di=sub.Di)
     gidx = cpu(lay.idx[ri])
     check_topk_sets(gidx, ref_scores, sub.q_pos, case.k)
     for g in range(case.layers):
@@ -80,21 +80,26 @@ def run_and_check(name, seqs, rows_in_seq):
     return case, sub
 
 
-def test_decode_32k_sampled_rows():
-    run_and_check("decode_32k", seqs=[0, 17, 31], rows_in_seq=[0])
+def test_decode_32k_every_row():
+    run_and_check("decode_32k", seqs=range(32), rows_in_seq=[0])
 
 
-def test_ragged_decode_sampled_rows():
+def test_ragged_decode_every_row():
     lengths = inputs.ragged_lengths(16, 1024, 200000, inputs.PRESETS["ragged_decode"]["seed"])
-    longest = int(np.argmax(lengths))
-    shortest = int(np.argmin(lengths))
-    case, sub = run_and_check("ragged_decode", seqs=sorted({longest, shortest, 5}), rows_in_seq=[0])
-    assert max(sub.lengths) > 100000  # the long tail is covered
+    case, sub = run_and_check("ragged_decode", seqs=range(16), rows_in_seq=[0])
+    assert max(sub.lengths) > 100000 and min(sub.lengths) < 2048  # long tail and dense rows
+
+
+# chunked prefill rows at q_pos = 57344 + i: groups of four rows share a tensor-core tile
+# (edges between rows 3|4 and 4095|4096), and a row's causal edge falls on a 128-key tile
+# boundary when 57345 + i is a multiple of 128 (i = 127, 255, ...)
+PREFILL_ROWS = [0, 1, 2, 3, 4, 126, 127, 128, 129, 2047, 2048, 4095, 4096, 6143, 8188, 8189,
+                8190, 8191]
 
 
 def test_prefill_8k_sampled_rows():
-    run_and_check("prefill_8k", seqs=[0], rows_in_seq=[0, 4095, 8191])
+    run_and_check("prefill_8k", seqs=[0], rows_in_seq=PREFILL_ROWS)
 
 
 def test_indexshare_paged_sampled_rows():
-    run_and_check("indexshare_paged", seqs=[0, 63], rows_in_seq=[0])
+    run_and_check("indexshare_paged", seqs=[0, 1, 31, 32, 62, 63], rows_in_seq=[0])

@@ -42,12 +42,14 @@ def test_slowest_rank_sets_the_job_time(tmp_path):
         dist.barrier()
         ms = bench.max_over_ranks(10.0 + 5.0 * rank, world)   # rank 1 is the slow one
         rate = bench.job_rate(32, world, ms)
-        print(json.dumps({"rank": rank, "world": world, "ms": ms, "rate": rate}), flush=True)
+        # one file per rank: the launcher merges the ranks' stdout, lines may interleave
+        with open(os.path.join(sys.argv[1], f"rank{rank}.json"), "w") as f:
+            json.dump({"rank": rank, "world": world, "ms": ms, "rate": rate}, f)
         dist.destroy_process_group()
     '''))
-    r = torchrun([str(script)], tmp_path)
+    r = torchrun([str(script), str(tmp_path)], tmp_path)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    lines = [json.loads((tmp_path / f"rank{i}.json").read_text()) for i in range(2)]
     assert sorted(d["rank"] for d in lines) == [0, 1]
     for d in lines:
         assert d["world"] == 2 and d["ms"] == 15.0
