@@ -186,6 +186,152 @@ def job_rate(units_per_rank, world, ms):
     return world * units_per_rank / (ms * 1e-3)
 
 
+def pack_io(lay):
+    """Lay the step's per-query inputs (q8, q_scale, w, q_pos and every layer's q) and its
+    outputs (every layer's out and lse) out as views of two contiguous device buffers, so
+    that a step's upload and download are one copy each.  Returns (in_buf, out_buf)."""
+    import torch
+    c = lay.case
+    dev = c.k8.device
+
+    def layout(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            n = (n + 255) // 256 * 256
+            offs.append(n)
+            n += t.numel() * t.element_size()
+        return offs, n
+
+    ins = [c.q8, c.q_scale, c.w, c.q_pos] + list(c.q)
+    offs, n = layout(ins)
+    in_buf = torch.empty(n, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(ins, offs):
+        v = in_buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    c.q8, c.q_scale, c.w, c.q_pos = views[:4]
+    c.q = views[4:]
+    outs = list(lay.out) + list(lay.lse)
+    offs, n = layout(outs)
+    out_buf = torch.empty(n, dtype=torch.uint8, device=dev)
+    ov = [out_buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+          for t, o in zip(outs, offs)]
+    lay.out, lay.lse = ov[:len(lay.out)], ov[len(lay.out):]
+    return in_buf, out_buf
+
+
+def kernel_times(layers, stream, steps, fns):
+    """Average device time of each call type: `steps` launches of one call (inputs rotating
+    over the layers' input sets) captured into one CUDA graph and replayed between two
+    events on the launching stream, so that host submission does not read as device time.
+    An eager loop stands in where capture is unavailable."""
+    import torch
+    out = []
+    for fn in fns:
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        try:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                for lay in layers:
+                    lay.stream = cap
+                fn(layers[0])
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    for i in range(steps):
+                        fn(layers[i % len(layers)])
+            for lay in layers:
+                lay.stream = None
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+        except Exception:
+            for lay in layers:
+                lay.stream = None
+            torch.cuda.synchronize()
+            a.record(stream)
+            for i in range(steps):
+                fn(layers[i % len(layers)])
+            b.record(stream)
+            torch.cuda.synchronize()
+        out.append(a.elapsed_time(b) / steps)
+    return out
+
+
+def step_of(case):
+    return (lambda lay: lay.run_shared()) if case.layers > 1 else (lambda lay: lay.run())
+
+
+def time_steps(layers, stream, steps, warmup, step):
+    """Milliseconds per whole step: `steps` steps back to back between two events."""
+    import torch
+    for i in range(warmup):
+        step(layers[i % len(layers)])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        step(layers[i % len(layers)])
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def measure_other_workload(name, dev, steps, warmup, hbm_peak, bf16_peak):
+    """One of the other serving workloads, measured beside the headline one (not part of
+    `value`): whole-step time, per-kernel times and the roofline that bounds the step."""
+    import torch
+    from sparse_attention_29_b300.pipeline import DsaLayer
+    n_sets = 1 if name in ("prefill_8k", "indexshare_paged") else 2
+    sets = [make_workload(name, dev, seed_offset=17 * i) for i in range(n_sets)]
+    layers = [DsaLayer(c) for c in sets]
+    case = sets[0]
+    stream = torch.cuda.current_stream()
+    step = step_of(case)
+    ms = time_steps(layers, stream, steps, warmup, step)
+    mla = (lambda lay: lay.mla_shared()) if case.layers > 1 else (lambda lay: lay.mla())
+    k_idx, k_topk, k_mla = kernel_times(layers, stream, steps,
+                                        [lambda lay: lay.indexer(), lambda lay: lay.topk(), mla])
+    layers[0].check_device_error()
+    b_idx, b_topk, b_mla = per_query_bytes(case)
+    res = {"workload": name + ": " + WORKLOADS[name], "rows": case.rows, "steps": steps,
+           "ms_per_step": ms, "query_tok_per_s": case.rows / (ms * 1e-3),
+           "kernel_ms": {"indexer": k_idx, "topk": k_topk, "sparse_mla": k_mla}}
+    if case.T > 1:
+        # chunked prefill: the indexer is a dense fp8 contraction (every visible key's q.k
+        # dot products), the sparse MLA two bf16 contractions per selected key
+        flops = float(case.q_pos.long().add(1).sum().item()) * case.Hi * case.Di * 2.0
+        fp8_peak = 2.0 * bf16_peak
+        tf = flops / (k_idx * 1e-3) / 1e12
+        nsel = float(case.q_pos.long().add(1).clamp(max=case.k).sum().item())
+        mla_flops = nsel * case.H * (2.0 * (case.d + case.r) + 2.0 * case.d)
+        mtf = mla_flops / (k_mla * 1e-3) / 1e12
+        res["roofline"] = {"bound": "tensor", "kernel": "indexer", "achieved": tf,
+                           "peak": fp8_peak, "unit": "TFLOP/s", "frac": tf / fp8_peak,
+                           "algorithmic_flops": flops,
+                           "peak_source": "measured bf16 burst x 2 (nominal fp8:bf16 ratio)"}
+        res["sparse_mla_roofline"] = {"bound": "tensor", "achieved": mtf, "peak": bf16_peak,
+                                      "unit": "TFLOP/s", "frac": mtf / bf16_peak,
+                                      "algorithmic_flops": mla_flops}
+        res["score_round_trip_bytes"] = scores_in_step(case)
+    else:
+        step_bytes = b_idx + b_topk + b_mla - scores_in_step(case)
+        tbs = step_bytes / (ms * 1e-3) / 1e12
+        res["roofline"] = {"bound": "hbm", "kernel": "whole step", "achieved": tbs * 1e3,
+                           "peak": hbm_peak, "unit": "GB/s", "frac": tbs * 1e3 / hbm_peak,
+                           "algorithmic_bytes": step_bytes}
+        res["us_per_step"] = ms * 1e3
+    del layers, sets
+    torch.cuda.empty_cache()
+    return res
+
+
 def make_workload(name, device, seed_offset=0):
     from sparse_attention_29_b300 import inputs
     return inputs.preset(name, seed=inputs.PRESETS[name]["seed"] + seed_offset, device=device)
@@ -331,6 +477,8 @@ def main():
     ap.add_argument("--sets", type=int, default=3, help="rotating input sets")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads measured beside the decode batch")
     ap.add_argument("--profile", action="store_true",
                     help="lean run for profiler captures: one input set, no clock pre-roll, "
                          "no per-kernel loops, graph replay, e2e or CPU baseline")
@@ -382,7 +530,11 @@ def main():
         else:
             lay.run()
 
-    launches_per_step = 3 + (1 if layers[0].ws_bytes else 0)
+    # indexer, top-k and sparse MLA; split rows merge inside the MLA kernel's clusters, and
+    # a separate merge kernel runs only when a row needs more splits than a cluster holds
+    # (fewer than SMs / 8 rows)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches_per_step = 3 + (1 if layers[0].ws_bytes and case.rows * 8 < sms else 0)
     for i in range(args.warmup):
         step(layers[i % len(layers)])
     torch.cuda.synchronize()
@@ -414,48 +566,13 @@ def main():
     layers[0].check_device_error()
 
     # ---- per-kernel durations: each call type launched K times back to back (its inputs
-    # are the previous steps' outputs), captured into one CUDA graph and replayed, so that
-    # the host's per-call submission cost does not read as device time; events on the
-    # launching stream around the replay, average per launch --------------------------
-    def time_calls(fn):
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        try:
-            cap = torch.cuda.Stream()
-            cap.wait_stream(stream)
-            with torch.cuda.stream(cap):
-                for lay in layers:
-                    lay.stream = cap
-                fn(layers[0])
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
-                    for i in range(args.steps):
-                        fn(layers[i % len(layers)])
-            for lay in layers:
-                lay.stream = None
-            g.replay()
-            torch.cuda.synchronize()
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-        except Exception:  # no capture: an eager loop (includes host submission time)
-            for lay in layers:
-                lay.stream = None
-            torch.cuda.synchronize()
-            a.record(stream)
-            for i in range(args.steps):
-                fn(layers[i % len(layers)])
-            b.record(stream)
-            torch.cuda.synchronize()
-        return a.elapsed_time(b) / args.steps
-
+    # are the previous steps' outputs), graph-replayed between events (kernel_times) ------
     if args.profile:  # no further launches after the timed steps
-        time_calls = lambda fn: float("nan")  # noqa: E731
-    k_idx = time_calls(lambda lay: lay.indexer())
-    k_topk = time_calls(lambda lay: lay.topk())
-    k_mla = time_calls(lambda lay: lay.mla_shared() if shared else lay.mla())
+        k_idx = k_topk = k_mla = float("nan")
+    else:
+        mla_call = (lambda lay: lay.mla_shared()) if shared else (lambda lay: lay.mla())
+        k_idx, k_topk, k_mla = kernel_times(
+            layers, stream, args.steps, [lambda lay: lay.indexer(), lambda lay: lay.topk(), mla_call])
 
     # ---- the same K steps replayed from a CUDA graph of the C-ABI calls ----------------
     graph_ms = None
@@ -499,27 +616,19 @@ def main():
     value = job_rate(q_tokens, world, ms_per_step)
 
     # ---- e2e: host (pinned) inputs -> C-ABI calls -> host result, every step ----------
+    # A serving loop's pipeline: each input set's per-query inputs live in one pinned host
+    # buffer and one device buffer (views of it feed the calls), its outputs likewise, so
+    # a step is one upload, the C-ABI calls and one download.  The upload of a step runs on
+    # one copy stream and the download of the previous one on another while a step
+    # computes; events keep a set's buffers from being reused before the step that last
+    # used them (and the download of its outputs) is done.
     e2e = None
     if not args.no_e2e:
-        host_in = []
-        for c in sets:
-            h = {"q8": c.q8.cpu().pin_memory(), "q_scale": c.q_scale.cpu().pin_memory(),
-                 "w": c.w.cpu().pin_memory(), "q_pos": c.q_pos.cpu().pin_memory(),
-                 "q": [q.cpu().pin_memory() for q in c.q]}
-            host_in.append(h)
-        host_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in lay.out]
-                    for lay in layers]
-        host_lse = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in lay.lse]
-                    for lay in layers]
-        h2d = sum(x.numel() * x.element_size() for x in
-                  (host_in[0]["q8"], host_in[0]["q_scale"], host_in[0]["w"], host_in[0]["q_pos"]))
-        h2d += sum(q.numel() * q.element_size() for q in host_in[0]["q"])
-        d2h = sum(o.numel() * o.element_size() for o in host_out[0] + host_lse[0])
-
-        # a serving loop's pipeline: the inputs of a step are uploaded on one copy stream
-        # and the outputs of the previous step downloaded on another while a step computes;
-        # events keep each input set's buffers from being overwritten before the step
-        # that last used them (and the download of its outputs) has finished
+        packed = [pack_io(lay) for lay in layers]
+        host_in = [ib.cpu().pin_memory() for ib, _ in packed]
+        host_out = [torch.empty(ob.shape, dtype=ob.dtype).pin_memory() for _, ob in packed]
+        h2d = packed[0][0].numel()
+        d2h = packed[0][1].numel()
         n_sets = len(layers)
         h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
         computed = [torch.cuda.Event() for _ in range(n_sets)]
@@ -529,29 +638,21 @@ def main():
 
         def e2e_step(i):
             j = i % n_sets
-            c, lay, h = sets[j], layers[j], host_in[j]
+            (in_dev, out_dev), lay = packed[j], layers[j]
+            if used[j]:
+                h2d_stream.wait_event(computed[j])
             with torch.cuda.stream(h2d_stream):
-                if used[j]:
-                    h2d_stream.wait_event(computed[j])
-                c.q8.copy_(h["q8"], non_blocking=True)
-                c.q_scale.copy_(h["q_scale"], non_blocking=True)
-                c.w.copy_(h["w"], non_blocking=True)
-                c.q_pos.copy_(h["q_pos"], non_blocking=True)
-                for qd, qh in zip(c.q, h["q"]):
-                    qd.copy_(qh, non_blocking=True)
-                uploaded[j].record(h2d_stream)
+                in_dev.copy_(host_in[j], non_blocking=True)
+            uploaded[j].record(h2d_stream)
             stream.wait_event(uploaded[j])
             if used[j]:
                 stream.wait_event(downloaded[j])
             step(lay)
             computed[j].record(stream)
+            d2h_stream.wait_event(computed[j])
             with torch.cuda.stream(d2h_stream):
-                d2h_stream.wait_event(computed[j])
-                for od, oh in zip(lay.out, host_out[j]):
-                    oh.copy_(od, non_blocking=True)
-                for od, oh in zip(lay.lse, host_lse[j]):
-                    oh.copy_(od, non_blocking=True)
-                downloaded[j].record(d2h_stream)
+                host_out[j].copy_(out_dev, non_blocking=True)
+            downloaded[j].record(d2h_stream)
             used[j] = True
 
         for i in range(args.warmup):
@@ -563,16 +664,20 @@ def main():
         s2.record(stream)
         h2d_stream.wait_stream(stream)
         d2h_stream.wait_stream(stream)
+        t_host = time.perf_counter()
         for i in range(args.steps):
             e2e_step(i)
+        host_us = (time.perf_counter() - t_host) / args.steps * 1e6
         stream.wait_stream(d2h_stream)
         e2.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(s2.elapsed_time(e2), world, dev) / args.steps
+        layers[0].check_device_error()
         e2e = {"value": job_rate(q_tokens, world, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "pipelined": "inputs uploaded and outputs downloaded on two copy streams "
-                            "while a step computes (pinned host buffers)"}
+               "host_submit_us_per_step": host_us,
+               "pipelined": "one packed upload and one packed download per step (pinned host "
+                            "buffers), on two copy streams while a step computes"}
 
     if rank != 0:
         if world > 1:
@@ -629,6 +734,16 @@ def main():
             line["cache_append"] = time_cache_append(dev, hbm_peak)
         except Exception as exc:
             line["cache_append"] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+    if not args.profile and world == 1 and not args.no_extras and args.workload == "decode_32k":
+        # the other serving workloads, each measured on its own (not part of `value`)
+        others = {}
+        for name in ("prefill_8k", "ragged_decode", "indexshare_paged"):
+            try:
+                others[name] = measure_other_workload(name, dev, max(5, min(args.steps, 20)),
+                                                      3, hbm_peak, bf16_peak)
+            except Exception as exc:
+                others[name] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+        line["other_workloads"] = others
     if cpu_base:
         line["cpu_baseline"] = cpu_base
     if args.profile:
