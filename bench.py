@@ -320,6 +320,17 @@ def measure_other_workload(name, dev, steps, warmup, hbm_peak, bf16_peak):
                                       "unit": "TFLOP/s", "frac": mtf / bf16_peak,
                                       "algorithmic_flops": mla_flops}
         res["score_round_trip_bytes"] = scores_in_step(case)
+        # the same step with the fused indexer + top-k (no score matrix in memory)
+        ms_f = time_steps(layers, stream, steps, warmup, lambda lay: lay.run_fused())
+        (k_f,) = kernel_times(layers, stream, steps, [lambda lay: lay.indexer_topk()])
+        layers[0].check_device_error()
+        tf_f = flops / (k_f * 1e-3) / 1e12
+        res["fused_indexer_topk"] = {
+            "ms_per_step": ms_f, "query_tok_per_s": case.rows / (ms_f * 1e-3),
+            "indexer_topk_ms": k_f,
+            "roofline": {"bound": "tensor", "kernel": "indexer + top-k (fused)",
+                         "achieved": tf_f, "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": tf_f / fp8_peak, "algorithmic_flops": flops}}
     else:
         step_bytes = b_idx + b_topk + b_mla - scores_in_step(case)
         tbs = step_bytes / (ms * 1e-3) / 1e12
@@ -520,6 +531,9 @@ def main():
     sets = [make_workload(args.workload, dev, seed_offset=1000 * rank + 17 * i)
             for i in range(args.sets)]
     layers = [DsaLayer(c) for c in sets]
+    # every set's per-query inputs and outputs as views of one device buffer each (the
+    # end-to-end measurement moves each with one copy)
+    packed = [pack_io(lay) for lay in layers]
     case = sets[0]
     shared = case.layers > 1
     stream = torch.cuda.current_stream()
@@ -576,6 +590,7 @@ def main():
 
     # ---- the same K steps replayed from a CUDA graph of the C-ABI calls ----------------
     graph_ms = None
+    graphs = None
     try:
         if args.profile:
             raise RuntimeError("skipped in a profile run")
@@ -607,6 +622,7 @@ def main():
         layers[0].check_device_error()
     except Exception as exc:  # graphs are an extra measurement; the step time stands
         graph_ms = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+        graphs = None
         for lay in layers:
             lay.stream = None
 
@@ -618,13 +634,15 @@ def main():
     # ---- e2e: host (pinned) inputs -> C-ABI calls -> host result, every step ----------
     # A serving loop's pipeline: each input set's per-query inputs live in one pinned host
     # buffer and one device buffer (views of it feed the calls), its outputs likewise, so
-    # a step is one upload, the C-ABI calls and one download.  The upload of a step runs on
-    # one copy stream and the download of the previous one on another while a step
-    # computes; events keep a set's buffers from being reused before the step that last
-    # used them (and the download of its outputs) is done.
+    # a step is one upload, the C-ABI calls and one download.  As a serving loop does, the
+    # C-ABI calls of each input set's step are captured once into a CUDA graph and the
+    # graph is replayed per step (host submission per step: one launch instead of three
+    # calls).  The upload of a step runs on one copy stream and the download of the
+    # previous one on another while a step computes; events keep a set's buffers from
+    # being reused before the step that last used them (and the download of its outputs)
+    # is done.
     e2e = None
     if not args.no_e2e:
-        packed = [pack_io(lay) for lay in layers]
         host_in = [ib.cpu().pin_memory() for ib, _ in packed]
         host_out = [torch.empty(ob.shape, dtype=ob.dtype).pin_memory() for _, ob in packed]
         h2d = packed[0][0].numel()
@@ -647,7 +665,10 @@ def main():
             stream.wait_event(uploaded[j])
             if used[j]:
                 stream.wait_event(downloaded[j])
-            step(lay)
+            if graphs is not None:
+                graphs[j].replay()
+            else:
+                step(lay)
             computed[j].record(stream)
             d2h_stream.wait_event(computed[j])
             with torch.cuda.stream(d2h_stream):
@@ -677,7 +698,10 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "host_submit_us_per_step": host_us,
                "pipelined": "one packed upload and one packed download per step (pinned host "
-                            "buffers), on two copy streams while a step computes"}
+                            "buffers), on two copy streams while a step computes",
+               "step_submission": ("the C-ABI calls of each input set's step captured once "
+                                   "into a CUDA graph, replayed per step") if graphs is not None
+                                  else "the C-ABI calls, eagerly"}
 
     if rank != 0:
         if world > 1:

@@ -114,6 +114,33 @@ dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int L
                       int32_t *idx, void *stream);
 
 /*
+ * Fused lightning indexer + causal top-K for chunked prefill (§Lightning Indexer; the
+ * indexer "becomes the visible bottleneck" once attention is sparse: remio.ai, the
+ * section on IndexShare).  Computes exactly what dsa_indexer_scores followed by dsa_topk
+ * computes (same scores, same selection and tie rule, same output idx [B*T, k]), but the
+ * [B*T, Lmax] score matrix never reaches memory: each query group's rows are scored and
+ * selected on one SM, which keeps per row a coarse histogram of the scores it keeps and a
+ * running threshold (the bin of the row's k-th best score so far), and appends to the
+ * row's candidate list (in `workspace`) only scores at or above it; a second kernel
+ * ranks the candidates of the row's final bin and writes the selection in ascending
+ * token order.  Arguments as dsa_indexer_scores and dsa_topk.
+ * workspace: at least dsa_indexer_topk_workspace_bytes(B, T, Lmax) bytes, 16-byte
+ * aligned (candidate slots for every visible token of every row, and per-row counts);
+ * typically a small part of it is written.
+ * Supported: as dsa_indexer_scores with ceil(Hi/16)*16 == 64 (four query rows of 64
+ * heads per tensor-core tile); 1 <= k <= 8192.  Meant for many query rows per sequence (each SM
+ * owns whole query groups); decode batches are better served by the two separate calls.
+ */
+dsa_status_t dsa_indexer_topk(const uint8_t *q8, const float *q_scale, const float *w,
+                              const uint8_t *k8_cache, const float *k_scale,
+                              const dsa_cache_layout_t *layout, const int32_t *q_pos, int B,
+                              int T, int Hi, int Di, int Lmax, int k, int32_t *idx,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of dsa_indexer_topk ((size_t)-1 for invalid sizes). */
+size_t dsa_indexer_topk_workspace_bytes(int B, int T, int Lmax);
+
+/*
  * Sparse MLA decode in MQA / absorbed mode (§Sparse MLA, §MLA changes), one query row per
  * sequence.  For sequence b and head h, over the valid entries j of idx[b, :] (-1 skips):
  *   logit_j = scale * q[b,h,:] . c_j[:]            (c_j = cached row of token idx[b,j],

@@ -26,7 +26,7 @@ DSA_NOALLOC_SCRATCH_BYTES = 20 << 20
 EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
            "dsa_sparse_mla_decode", "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_prefill",
            "dsa_sparse_mla_shared", "dsa_cache_append", "dsa_workspace_bytes",
-           "dsa_device_error")
+           "dsa_device_error", "dsa_indexer_topk", "dsa_indexer_topk_workspace_bytes")
 
 
 class DsaError(RuntimeError):
@@ -64,6 +64,10 @@ def load(path: str = LIB_PATH):
     lib.dsa_indexer_scores.argtypes = [P, P, P, P, P, LP, P, I, I, I, I, I, P, P]
     lib.dsa_topk.restype = I
     lib.dsa_topk.argtypes = [P, P, I, I, I, P, P]
+    lib.dsa_indexer_topk.restype = I
+    lib.dsa_indexer_topk.argtypes = [P, P, P, P, P, LP, P, I, I, I, I, I, I, P, P, S, P]
+    lib.dsa_indexer_topk_workspace_bytes.restype = S
+    lib.dsa_indexer_topk_workspace_bytes.argtypes = [I, I, I]
     lib.dsa_sparse_mla_decode.restype = I
     lib.dsa_sparse_mla_decode.argtypes = [P, P, LP, P, I, I, I, I, I, F, P, P, P, S, P]
     lib.dsa_sparse_mla_decode_noalloc.restype = I
@@ -127,6 +131,22 @@ def dsa_indexer_scores(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, H
 def dsa_topk(scores, q_pos, rows, Lmax, k, idx, stream=None):
     st = load().dsa_topk(_ptr(scores), _ptr(q_pos), rows, Lmax, k, _ptr(idx), _stream(stream))
     _check("dsa_topk", st)
+
+
+def dsa_indexer_topk(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, Hi, Di, Lmax, k,
+                     idx, workspace, workspace_bytes, stream=None):
+    st = load().dsa_indexer_topk(_ptr(q8), _ptr(q_scale), _ptr(w), _ptr(k8_cache), _ptr(k_scale),
+                                 ctypes.byref(layout), _ptr(q_pos), B, T, Hi, Di, Lmax, k,
+                                 _ptr(idx), _ptr(workspace), int(workspace_bytes),
+                                 _stream(stream))
+    _check("dsa_indexer_topk", st)
+
+
+def dsa_indexer_topk_workspace_bytes(B, T, Lmax) -> int:
+    n = load().dsa_indexer_topk_workspace_bytes(B, T, Lmax)
+    if n == ctypes.c_size_t(-1).value:
+        raise DsaError("dsa_indexer_topk_workspace_bytes", 1)
+    return n
 
 
 def dsa_cache_append(k_new, c_new, seq, pos, n, B, Di, D, layout, k8_cache, k_scale, kv_cache,

@@ -225,17 +225,24 @@ const char *dsa_status_string(dsa_status_t s) {
     return "unknown status";
 }
 
-dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const float *w,
-                                const uint8_t *k8_cache, const float *k_scale,
-                                const dsa_cache_layout_t *layout, const int32_t *q_pos,
-                                int B, int T, int Hi, int Di, int Lmax, float *scores,
-                                void *stream) {
-    if (!q8 || !q_scale || !w || !k8_cache || !k_scale || !q_pos || !scores)
+}  // extern "C"
+
+namespace {
+
+// Shared by the indexer entry points: checks, launch parameters and tensor maps, launch.
+dsa_status_t indexer_common(const uint8_t *q8, const float *q_scale, const float *w,
+                            const uint8_t *k8_cache, const float *k_scale,
+                            const dsa_cache_layout_t *layout, const int32_t *q_pos, int B,
+                            int T, int Hi, int Di, int Lmax, float *scores, int k,
+                            uint2 *cand, int64_t cap, uint4 *meta, void *stream) {
+    const bool sel = cand != nullptr;
+    if (!q8 || !q_scale || !w || !k8_cache || !k_scale || !q_pos || (!sel && !scores))
         return DSA_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || Hi <= 0 || Di <= 0 || Lmax <= 0) return DSA_ERR_INVALID_ARG;
     if (Di != 32 && Di != 64 && Di != 128) return DSA_ERR_UNSUPPORTED;
     const int HP = (Hi + 15) / 16 * 16;
     if (HP > 256) return DSA_ERR_UNSUPPORTED;
+    if (sel && HP != 64) return DSA_ERR_UNSUPPORTED;  // four 64-head rows per tile
     if (!aligned16(q8) || !aligned16(k8_cache)) return DSA_ERR_INVALID_ARG;
     if (!layout_ok(layout, B, true)) return DSA_ERR_INVALID_ARG;
     if ((int64_t)layout->num_rows >= ((int64_t)1 << 31) - 256) return DSA_ERR_UNSUPPORTED;
@@ -265,6 +272,11 @@ dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const f
     p.acc_cols = pow2_at_least(p.N);
     p.num_acc = 512 / p.acc_cols;  // every TMEM column: the MMA never waits on the epilogue
     if (p.num_acc > 8) p.num_acc = 8;
+    p.sel = sel ? 1 : 0;
+    p.k = k;
+    p.cap = cap;
+    p.cand = cand;
+    p.meta = meta;
 
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_tiled();
     if (!encode) return DSA_ERR_CUDA;
@@ -301,6 +313,60 @@ dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const f
     const int sms = current_sm_count();
     if (sms <= 0) return DSA_ERR_CUDA;
     return from_cuda(launch_indexer(p, kmap, kmap128, qmap, sms, static_cast<cudaStream_t>(stream)));
+}
+
+// Workspace of dsa_indexer_topk: candidate lists (Lmax rounded up to a multiple of 128
+// slots of 8 bytes per row: four quarters, one per epilogue warp, each holding the 32 of
+// every 128 keys that warp scores), then per-row counts (32 bytes per row).
+int64_t cand_slots(int Lmax) { return ((int64_t)Lmax + 127) / 128 * 128; }
+
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const float *w,
+                                const uint8_t *k8_cache, const float *k_scale,
+                                const dsa_cache_layout_t *layout, const int32_t *q_pos,
+                                int B, int T, int Hi, int Di, int Lmax, float *scores,
+                                void *stream) {
+    return indexer_common(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, Hi, Di, Lmax,
+                          scores, 0, nullptr, 0, nullptr, stream);
+}
+
+size_t dsa_indexer_topk_workspace_bytes(int B, int T, int Lmax) {
+    if (B <= 0 || T <= 0 || Lmax <= 0) return (size_t)-1;
+    const int64_t rows = (int64_t)B * T;
+    return (size_t)(rows * cand_slots(Lmax) * 8 + rows * 32);
+}
+
+dsa_status_t dsa_indexer_topk(const uint8_t *q8, const float *q_scale, const float *w,
+                              const uint8_t *k8_cache, const float *k_scale,
+                              const dsa_cache_layout_t *layout, const int32_t *q_pos, int B,
+                              int T, int Hi, int Di, int Lmax, int k, int32_t *idx,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    if (!idx || !workspace) return DSA_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || Lmax <= 0 || k <= 0) return DSA_ERR_INVALID_ARG;
+    if (k > 8192) return DSA_ERR_UNSUPPORTED;
+    const size_t need = dsa_indexer_topk_workspace_bytes(B, T, Lmax);
+    if (workspace_bytes < need) return DSA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)B * T;
+    const int64_t cap = cand_slots(Lmax);
+    uint2 *cand = static_cast<uint2 *>(workspace);
+    uint4 *meta = reinterpret_cast<uint4 *>(cand + rows * cap);
+    dsa_status_t st = indexer_common(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, Hi,
+                                     Di, Lmax, nullptr, k, cand, cap, meta, stream);
+    if (st != DSA_OK) return st;
+    TopkCandParams tp;
+    tp.cand = cand;
+    tp.meta = meta;
+    tp.q_pos = q_pos;
+    tp.idx = idx;
+    tp.rows = (int)rows;
+    tp.Lmax = Lmax;
+    tp.k = k;
+    tp.cap = cap;
+    return from_cuda(launch_topk_cand(tp, static_cast<cudaStream_t>(stream)));
 }
 
 dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int Lmax, int k,

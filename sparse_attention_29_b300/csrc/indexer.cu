@@ -27,6 +27,7 @@
 // global load.  CTAs are persistent: the tiles of all query groups form one list and
 // each CTA takes a contiguous slice of it, so ragged contexts balance evenly.
 #include "internal.h"
+#include "keys.cuh"
 #include "ptx.cuh"
 
 namespace dsa {
@@ -57,11 +58,12 @@ constexpr int kBoxRows = 64;
 
 struct Smem {
     // offsets (bytes) from the 1024-aligned dynamic shared memory base
-    uint32_t kstage, qbuf, qbuf_bytes, ksring, wbuf, gpos, prefix, bars, total;
+    uint32_t kstage, qbuf, qbuf_bytes, ksring, wbuf, gpos, prefix, sel, bars, total;
     int ring;
 };
 
 constexpr int kBatch = 32;  // tiles the producer resolves at once (one lane per tile)
+constexpr int kStageSlots = 64;  // fused selection: staged candidates per (row, warp)
 
 // Key-scale ring slots.  The producer fills a tile's slot when it issues the tile's key
 // load, after the stage-free wait for tile (it - stages); by then the epilogue has
@@ -70,8 +72,10 @@ __host__ __device__ inline int ks_ring_slots(int stages, int num_acc) {
     return stages + num_acc + 1;
 }
 
+// sel_rows: query rows per group whose fused selection state (a coarse histogram and
+// three counters per row) the CTA keeps; 0 without fused selection.
 __host__ __device__ inline Smem smem_layout(int Di, int N, int stages, int num_groups,
-                                            int num_acc) {
+                                            int num_acc, int sel_rows) {
     Smem s;
     s.ring = ks_ring_slots(stages, num_acc);
     uint32_t off = 0;
@@ -88,8 +92,12 @@ __host__ __device__ inline Smem smem_layout(int Di, int N, int stages, int num_g
     off += 2 * 16 * 4;
     s.prefix = off;
     off += ((uint32_t)num_groups + 1 + 3) / 4 * 16;
+    s.sel = off;  // [rows][kCoarseBins] counts, [4][16] per-row counters, staging
+    off += (uint32_t)sel_rows * kCoarseBins * 4 + (sel_rows ? 4 * 16 * 4 : 0);
+    off = (off + 15) & ~15u;
+    off += (uint32_t)sel_rows * 4 * kStageSlots * 8;  // [row][warp][kStageSlots] (key, index)
     s.bars = off;
-    off += (uint32_t)(2 * stages + 4 + 2 * num_acc + 1 + s.ring) * 8 + 16;  // + flag, tmem
+    off += (uint32_t)(2 * stages + 4 + 2 * num_acc + 1 + s.ring + 1) * 8 + 16;  // + flag, tmem
     s.total = off;
     return s;
 }
@@ -216,13 +224,50 @@ __device__ __forceinline__ uint64_t relu2(uint32_t a, uint32_t b) {
     return pack2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
 }
 
+// Raise row q's selection threshold (a coarse bin) to the highest bin b whose count of
+// candidates at or above b reaches k.  One warp; the bins are read from the top down, 32
+// at a time.  Counts read while other warps still append are lower bounds, so the bin
+// found never passes the row's true k-th best: no score that can still be selected is
+// ever skipped.  With `exact` (no appends in flight) it returns the final bin and sets
+// *above to the count strictly above it and *at to the count in it; -1 if fewer than k.
+__device__ __forceinline__ int sel_scan(const volatile uint32_t *hist, int top, int floor_bin,
+                                        uint32_t k, uint32_t *above, uint32_t *at) {
+    const int lane = threadIdx.x & 31;
+    uint32_t acc = 0;
+    for (int b = top; b >= floor_bin; b -= 32) {
+        const int bin = b - lane;
+        const uint32_t c = bin >= floor_bin ? hist[bin] : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, acc + incl >= k);
+        if (hit) {
+            const int f = __ffs(hit) - 1;
+            const uint32_t inc_f = __shfl_sync(0xffffffffu, incl, f);
+            const uint32_t c_f = __shfl_sync(0xffffffffu, c, f);
+            if (above) *above = acc + inc_f - c_f;
+            if (at) *at = c_f;
+            return b - f;
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return -1;
+}
+
 // kW64: decode form (one query row of 64 padded heads per group); its weights stay in
 // registers.  Otherwise they are read from shared memory.
-template <int DI, bool kW64>
+// kSel: fused selection (several rows per group only): every CTA owns whole query groups
+// and keeps, per row, the candidates that can still be among the row's k best (see
+// dsa_indexer_topk) instead of storing scores.
+template <int DI, bool kW64, bool kSel>
 __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap kmap128,
                    const __grid_constant__ CUtensorMap qmap, const IndexerParams p) {
+    static_assert(!(kSel && kW64), "fused selection runs the several-rows epilogue");
     constexpr int kThreads = EpiCfg<kW64>::kThreads;
     constexpr int kEpiSets = EpiCfg<kW64>::kSets;
     constexpr int kEpiWarps = EpiCfg<kW64>::kWarps;
@@ -232,7 +277,7 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc);
+    const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc, kSel ? p.G : 0);
     uint8_t *kstage = smem + L.kstage;
     uint8_t *qbuf = smem + L.qbuf;
     float *ksring = (float *)(smem + L.ksring);
@@ -248,8 +293,18 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
     uint64_t *accempty = accfull + p.num_acc;
     uint64_t *drain = accempty + p.num_acc;
     uint64_t *ksfull = drain + 1;
-    volatile int *abort_flag = (volatile int *)(ksfull + L.ring);
-    uint32_t *tmem_base_sm = (uint32_t *)(ksfull + L.ring) + 1;
+    uint64_t *gsync = ksfull + L.ring;  // fused selection: group-end rounds of the epilogue
+    volatile int *abort_flag = (volatile int *)(gsync + 1);
+    uint32_t *tmem_base_sm = (uint32_t *)(gsync + 1) + 1;
+    // fused selection state of the current group's rows: coarse-bin counts of the
+    // candidates kept, and per row the candidates kept, the threshold bin and the highest
+    // bin seen
+    uint32_t *hist = (uint32_t *)(smem + L.sel);
+    uint32_t *sel_n = hist + (kSel ? p.G * kCoarseBins : 0);  // [row][quarter] counts
+    int *sel_t = (int *)(sel_n + 16);   // threshold bin
+    int *sel_top = sel_t + 16;          // highest bin kept
+    float *sel_f = (float *)(sel_top + 16);  // coarse_floor(threshold bin)
+    uint2 *stage = (uint2 *)(smem + ((L.sel + (uint32_t)(kSel ? p.G : 0) * kCoarseBins * 4 + 4 * 16 * 4 + 15) & ~15u));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -304,8 +359,22 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         __syncthreads();
     }
     const int total = prefix[p.num_groups];
-    const int tb = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
-    const int te = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+    int tb = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+    int te = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+    if constexpr (kSel) {
+        // whole groups: the groups whose first tile falls in this CTA's share of the list
+        auto first_group_from = [&](int t) {  // first g with prefix[g] >= t
+            int lo = 0, hi = p.num_groups;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (prefix[mid] < t) lo = mid + 1;
+                else hi = mid;
+            }
+            return lo;
+        };
+        tb = prefix[first_group_from(tb)];
+        te = prefix[first_group_from(te)];
+    }
     if (tb >= te) return;
     const int ntile = te - tb;
 
@@ -325,6 +394,7 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         }
         for (int i = 0; i < L.ring; ++i) mbar_init(&ksfull[i], 32);  // every producer lane
         mbar_init(drain, kMmaWarps);
+        mbar_init(gsync, kEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -336,6 +406,11 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         prefetch_tmap(&kmap);
         prefetch_tmap(&kmap128);
         if (p.q_tma) prefetch_tmap(&qmap);
+    }
+    if constexpr (kSel) {
+        const int words = p.G * kCoarseBins + 3 * 16;
+        for (int i = tid; i < words; i += kThreads) hist[i] = 0u;
+        if (tid < 16) sel_f[tid] = -INFINITY;
     }
     tc_fence_before();
     __syncthreads();
@@ -601,6 +676,65 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         int abuf = 0, kslot = 0, gcount = 0, slot = 0;
         uint32_t aphase = 0, ksphase = 0;
         int r0 = 0, nr = 0, gfirst = 0;  // current group: first row, rows, first tile (abs.)
+        uint32_t grounds = 0;            // fused selection: group-end rounds completed
+        const int ew = warp - 4;         // epilogue warp 0 .. kEpiWarps-1
+        // fused selection: keep (key, index) of a visible score of row q (warp-wide call)
+        // if its bin reaches the row's threshold `thr` (read once per tile: a threshold
+        // one tile old is lower, which only keeps more); counts its bin, and the warp's
+        // highest kept bin raises the row's highest bin
+        // Each of the four warps serving a row appends to its own quarter of the row's list
+        // (a warp sees 32 of every 128 keys, so a quarter of cap always holds them).  Kept
+        // candidates are staged in shared memory and go out 32 at a time: one coalesced
+        // 8-byte store per lane, and the 32 bin counts and the highest bin with every lane
+        // active.  Counts in registers, for the j-th row of this set: sel_stg[j] staged,
+        // sel_cnt[j] written to the list.
+        uint32_t sel_cnt[kSel ? 2 : 1] = {}, sel_stg[kSel ? 2 : 1] = {};
+        const int64_t seg = p.cap / 4;
+        // write out `n` (<= 32) staged entries of row q (this set's row j), keep the rest
+        auto sel_flush = [&](int q, int j, uint32_t n) {
+            uint2 *st = stage + (q * 4 + quarter) * kStageSlots;
+            const uint32_t cnt = j ? sel_cnt[1] : sel_cnt[0];
+            const uint32_t stg = j ? sel_stg[1] : sel_stg[0];
+            __syncwarp();
+            uint32_t ck = 0;
+            if ((uint32_t)lane < n) {
+                const uint2 e = st[lane];
+                ck = coarse_key(key_score(e.x));
+                if (cnt + lane < seg) p.cand[(int64_t)(r0 + q) * p.cap + quarter * seg + cnt + lane] = e;
+                atomicAdd(&hist[q * kCoarseBins + ck], 1u);
+            }
+            const uint32_t hi = __reduce_max_sync(0xffffffffu, ck);
+            if (lane == 0 && n) atomicMax(&sel_top[q], (int)hi);
+            __syncwarp();
+            uint2 rest = make_uint2(0u, 0u);  // the staged entries past the first n move down
+            const bool mv = (uint32_t)lane + n < stg;
+            if (mv) rest = st[lane + n];
+            __syncwarp();
+            if (mv) st[lane] = rest;
+            __syncwarp();
+            if (j) { sel_cnt[1] = cnt + n; sel_stg[1] = stg - n; }
+            else { sel_cnt[0] = cnt + n; sel_stg[0] = stg - n; }
+        };
+        auto sel_emit = [&](int q, int s, float sc, bool keep, float thr) {
+            const bool pass = keep && sc >= thr;
+            const uint32_t m = __ballot_sync(0xffffffffu, pass);
+            if (!m) return;
+            const int j = q >= kEpiSets ? 1 : 0;
+            const uint32_t stg = j ? sel_stg[1] : sel_stg[0];
+            if (pass) stage[(q * 4 + quarter) * kStageSlots + stg + __popc(m & ((1u << lane) - 1u))] =
+                make_uint2(full_key(sc), (uint32_t)s);
+            if (j) sel_stg[1] = stg + __popc(m);
+            else sel_stg[0] = stg + __popc(m);
+            if (stg + __popc(m) >= 32) sel_flush(q, j, 32);
+        };
+        // one group-end round: every epilogue warp arrives, then waits for all (bounded)
+        auto sel_round = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gsync);
+            const bool ok = mbar_wait(gsync, grounds & 1u, KID_INDEXER, abort_flag);
+            ++grounds;
+            return __all_sync(0xffffffffu, ok);
+        };
         for (int it = 0; it < ntile; ++it) {
             if (gw.at_start(it)) {
                 slot = gcount & 1;
@@ -650,13 +784,15 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                     if (s <= pos[0])
                         p.scores[(int64_t)r0 * p.Lmax + s] = (sum2(a01) + sum2(a23)) * ksc;
                 } else {
-                    // both sets work on every tile: set e takes query rows 2e and 2e+1, and
-                    // both rows' accumulators are loaded before one wait (tcgen05.wait::ld
-                    // covers every outstanding load); four independent chains per row
+                    // both sets work on every tile: set e takes query rows e, e + 2, ...
                     const float *wq = wbuf + slot * p.N;
-                    if (p.HP == 64) {
+                    if (kSel || p.HP == 64) {  // the fused selection runs 64-head rows only
                         // this set's rows one at a time: one 64-column load and wait each
                         for (int q = eset; q < nr; q += kEpiSets) {
+                            // fused selection: this row's threshold for the tile, and whether
+                            // the row selects at all (it sees more than k tokens)
+                            const float thr = kSel ? *(volatile float *)&sel_f[q] : 0.f;
+                            const bool keep_row = kSel && pos[q] + 1 > p.k;
                             uint32_t v0[64];
                             tmem_ld32(tacc + (uint32_t)(q * 64), *reinterpret_cast<uint32_t (*)[32]>(&v0[0]));
                             tmem_ld32(tacc + (uint32_t)(q * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&v0[32]));
@@ -669,9 +805,11 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                                 a01 = fma2(ww.x, relu2(v0[h + 0], v0[h + 1]), a01);
                                 a23 = fma2(ww.y, relu2(v0[h + 2], v0[h + 3]), a23);
                             }
-                            if (s <= pos[q]) p.scores[(int64_t)(r0 + q) * p.Lmax + s] = (sum2(a01) + sum2(a23)) * ksc;
+                            const float sc = (sum2(a01) + sum2(a23)) * ksc;
+                            if constexpr (kSel) sel_emit(q, s, sc, keep_row && s <= pos[q], thr);
+                            else if (s <= pos[q]) p.scores[(int64_t)(r0 + q) * p.Lmax + s] = sc;
                         }
-                    } else {
+                    } else if constexpr (!kSel) {
                         // other head counts: this set's rows one at a time, 32 heads per
                         // load (then 16 for the rest; HP is a multiple of 16)
                         for (int q = eset; q < nr; q += kEpiSets) {
@@ -706,10 +844,65 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&accempty[abuf]);
+                if constexpr (kSel) {
+                    // every sixteenth tile one warp of the set (in turn) raises the set's
+                    // rows' thresholds
+                    if ((it & 15) == 15 && ((it >> 4) & 3) == quarter) {
+                        for (int q = eset; q < nr; q += kEpiSets) {
+                            const int t_cur = *(volatile int *)&sel_t[q];
+                            const int tnew = sel_scan(hist + q * kCoarseBins,
+                                                      *(volatile int *)&sel_top[q], t_cur,
+                                                      (uint32_t)p.k, nullptr, nullptr);
+                            if (lane == 0 && tnew > t_cur) {
+                                *(volatile int *)&sel_t[q] = tnew;
+                                *(volatile float *)&sel_f[q] = coarse_floor(tnew);
+                            }
+                        }
+                    }
+                }
             }
             if (gw.is_last(it)) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&qempty[slot]);
+                if constexpr (kSel) {
+                    // the group's last tile: after every warp's appends, warp q finishes row q
+                    // (its final bin and counts to meta), then the state is cleared for the
+                    // next group; each step is a bounded round over all epilogue warps
+                    // this warp writes out what it still stages, then its counts of its rows'
+                    // list quarters go to shared memory for the finishing warp
+                    if (eset < nr) sel_flush(eset, 0, sel_stg[0]);
+                    if (eset + kEpiSets < nr) sel_flush(eset + kEpiSets, 1, sel_stg[1]);
+                    if (lane == 0) {
+                        if (eset < nr) sel_n[eset * 4 + quarter] = sel_cnt[0];
+                        if (eset + kEpiSets < nr) sel_n[(eset + kEpiSets) * 4 + quarter] = sel_cnt[1];
+                    }
+                    sel_cnt[0] = sel_stg[0] = 0;
+                    if constexpr (kSel) sel_cnt[1] = sel_stg[1] = 0;
+                    if (!sel_round()) break;
+                    if (ew < nr) {
+                        const int pq = gpos[slot * 16 + ew];
+                        if (pq >= 0 && pq + 1 > p.k) {
+                            uint32_t above = 0, at = 0;
+                            const int b0 = sel_scan(hist + ew * kCoarseBins, sel_top[ew], 0,
+                                                    (uint32_t)p.k, &above, &at);
+                            if (b0 < 0) record_error(KID_INDEXER, ERR_BAD_INDEX);
+                            if (lane == 0) {
+                                p.meta[2 * (r0 + ew)] = make_uint4(sel_n[ew * 4], sel_n[ew * 4 + 1],
+                                                                   sel_n[ew * 4 + 2], sel_n[ew * 4 + 3]);
+                                p.meta[2 * (r0 + ew) + 1] = make_uint4((uint32_t)max(b0, 0), above, at, 0u);
+                            }
+                        }
+                    }
+                    if (!sel_round()) break;
+                    const int words = nr * kCoarseBins;
+                    for (int i = ew * 32 + lane; i < words; i += kEpiWarps * 32) hist[i] = 0u;
+                    if (ew == 0 && lane < 16) {
+                        sel_t[lane] = 0;
+                        sel_top[lane] = 0;
+                        sel_f[lane] = -INFINITY;
+                    }
+                    if (!sel_round()) break;
+                }
             }
             gw.step(it);
             if (++abuf == p.num_acc) { abuf = 0; aphase ^= 1u; }
@@ -722,17 +915,26 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, (uint32_t)(p.acc_cols * p.num_acc));
 }
 
-template <int DI, bool kW64>
+template <int DI, bool kW64, bool kSel>
 cudaError_t launch_di(const IndexerParams &p, const CUtensorMap &kmap,
                       const CUtensorMap &kmap128, const CUtensorMap &qmap, int grid,
                       cudaStream_t stream) {
-    const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc);
+    const Smem L = smem_layout(DI, p.N, p.stages, p.num_groups, p.num_acc, kSel ? p.G : 0);
     const size_t bytes = L.total + 1024;
     static AttrCache attrs;
-    cudaError_t e = ensure_smem_attrs(attrs, indexer_kernel<DI, kW64>, (int)bytes);
+    cudaError_t e = ensure_smem_attrs(attrs, indexer_kernel<DI, kW64, kSel>, (int)bytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(indexer_kernel<DI, kW64>, dim3(grid), dim3(EpiCfg<kW64>::kThreads), bytes, stream, kmap,
-                      kmap128, qmap, p);
+    return launch_pdl(indexer_kernel<DI, kW64, kSel>, dim3(grid), dim3(EpiCfg<kW64>::kThreads),
+                      bytes, stream, kmap, kmap128, qmap, p);
+}
+
+template <int DI>
+cudaError_t launch_for_di(const IndexerParams &p, const CUtensorMap &kmap,
+                          const CUtensorMap &kmap128, const CUtensorMap &qmap, int grid,
+                          cudaStream_t stream) {
+    if (p.sel) return launch_di<DI, false, true>(p, kmap, kmap128, qmap, grid, stream);
+    if (p.N == 64 && p.G == 1) return launch_di<DI, true, false>(p, kmap, kmap128, qmap, grid, stream);
+    return launch_di<DI, false, false>(p, kmap, kmap128, qmap, grid, stream);
 }
 
 }  // namespace
@@ -743,22 +945,19 @@ cudaError_t launch_indexer(const IndexerParams &p_in, const CUtensorMap &kmap,
     IndexerParams p = p_in;
     // shared-memory budget: the key ring takes what the rest leaves, up to 12 stages
     const int budget = 227 * 1024 - 1024;
+    const int sel_rows = p.sel ? p.G : 0;
     p.stages = 12;  // ~192 KB in flight per SM keeps HBM busy across the ~3-6 us load latency
     while (p.stages >= 2 &&
-           (int)smem_layout(p.Di, p.N, p.stages, p.num_groups, p.num_acc).total > budget)
+           (int)smem_layout(p.Di, p.N, p.stages, p.num_groups, p.num_acc, sel_rows).total > budget)
         --p.stages;
     if (p.stages < 2) return cudaErrorInvalidConfiguration;
     const int64_t max_tiles = (int64_t)p.num_groups * ((p.Lmax + kTileKeys - 1) / kTileKeys);
     const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
     if (grid <= 0) return cudaSuccess;
-    const bool w64 = (p.N == 64 && p.G == 1);
     switch (p.Di) {
-        case 32: return w64 ? launch_di<32, true>(p, kmap, kmap128, qmap, grid, stream)
-                            : launch_di<32, false>(p, kmap, kmap128, qmap, grid, stream);
-        case 64: return w64 ? launch_di<64, true>(p, kmap, kmap128, qmap, grid, stream)
-                            : launch_di<64, false>(p, kmap, kmap128, qmap, grid, stream);
-        case 128: return w64 ? launch_di<128, true>(p, kmap, kmap128, qmap, grid, stream)
-                             : launch_di<128, false>(p, kmap, kmap128, qmap, grid, stream);
+        case 32: return launch_for_di<32>(p, kmap, kmap128, qmap, grid, stream);
+        case 64: return launch_for_di<64>(p, kmap, kmap128, qmap, grid, stream);
+        case 128: return launch_for_di<128>(p, kmap, kmap128, qmap, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }

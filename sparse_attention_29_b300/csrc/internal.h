@@ -97,6 +97,16 @@ struct IndexerParams {
     int num_acc;   // accumulator buffers
     int stages;    // key pipeline depth
     int q_tma;     // 1: query groups load by TMA (Hi == HP), 0: plain loads with padding
+    // fused selection (dsa_indexer_topk): instead of storing scores, each row keeps the
+    // candidates that can still be among its k best in cand[row * cap ..] as
+    // (full key, token index), in four quarters of cap / 4 slots (one per epilogue warp),
+    // and, at the end of its query group, meta[2 row] = the quarters' counts and
+    // meta[2 row + 1] = {final coarse bin B0, count above B0, count in B0, 0}
+    int sel;       // 1: fused selection
+    int k;
+    int64_t cap;   // candidate slots per row (>= Lmax)
+    uint2 *cand;
+    uint4 *meta;
 };
 
 // kmap: 64-row key boxes (any layout); kmap128: 128-row boxes (contiguous runs);
@@ -114,6 +124,18 @@ struct TopkParams {
 };
 
 cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream);
+
+// The final selection of the fused indexer + top-k: per row, from the candidates and the
+// counts the fused indexer left in cand / meta.
+struct TopkCandParams {
+    const uint2 *cand;
+    const uint4 *meta;
+    const int32_t *q_pos;
+    int32_t *idx;
+    int rows, Lmax, k;
+    int64_t cap;
+};
+cudaError_t launch_topk_cand(const TopkCandParams &p, cudaStream_t stream);
 
 // ---- sparse MLA -------------------------------------------------------------------
 constexpr int kMaxLayers = 8;

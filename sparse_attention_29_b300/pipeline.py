@@ -40,6 +40,7 @@ class DsaLayer:
         self.ws_bytes = max(ws1, wsg)
         self.workspace = (torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
                           if self.ws_bytes else None)
+        self.sel_ws = None  # dsa_indexer_topk's workspace, allocated on first use
 
     # -- the three calls ----------------------------------------------------------------
     def indexer(self):
@@ -50,6 +51,16 @@ class DsaLayer:
     def topk(self):
         c = self.case
         libdsa.dsa_topk(self.scores, c.q_pos, c.rows, c.Lmax, c.k, self.idx, self.stream)
+
+    def indexer_topk(self):
+        """The fused indexer + top-k (chunked prefill): the index set without the scores."""
+        c = self.case
+        if self.sel_ws is None:
+            n = libdsa.dsa_indexer_topk_workspace_bytes(c.B, c.T, c.Lmax)
+            self.sel_ws = torch.empty(n, dtype=torch.uint8, device=c.k8.device)
+        libdsa.dsa_indexer_topk(c.q8, c.q_scale, c.w, c.k8, c.k_scale, self.layout, c.q_pos,
+                                c.B, c.T, c.Hi, c.Di, c.Lmax, c.k, self.idx, self.sel_ws,
+                                self.sel_ws.numel(), self.stream)
 
     def mla(self, layer=0, idx=None):
         c = self.case
@@ -82,6 +93,11 @@ class DsaLayer:
         self.indexer()
         self.topk()
         self.mla_shared()
+
+    def run_fused(self, layer=0):
+        """Chunked prefill with the fused indexer + top-k, then sparse MLA."""
+        self.indexer_topk()
+        self.mla(layer)
 
     def check_device_error(self):
         st, code = libdsa.dsa_device_error(self.stream)

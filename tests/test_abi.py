@@ -99,3 +99,20 @@ def test_layout_keeps_its_tensors_alive():
     del t
     gc.collect()
     assert ref() is not None and layout.seq_start == ref().data_ptr()
+
+
+def test_fused_indexer_topk_checks_fail_before_any_launch(lib):
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 4
+    p = 0x1000
+    L2 = capi.CacheLayout(p, None, 0, 0, 100)
+    need = lib.dsa_indexer_topk_workspace_bytes(1, 16, 100)
+    assert need == 16 * 128 * 8 + 16 * 32
+    assert lib.dsa_indexer_topk_workspace_bytes(0, 16, 100) == ctypes.c_size_t(-1).value
+    args = (p, p, p, p, p, ctypes.byref(L2), p, 1, 16, 64, 128, 100, 32)
+    assert lib.dsa_indexer_topk(*args, None, p, need, None) == INVALID        # no output
+    assert lib.dsa_indexer_topk(*args, p, p, need - 16, None) == WORKSPACE    # too small
+    assert lib.dsa_indexer_topk(*args, p, p + 8, need, None) == INVALID       # misaligned
+    assert lib.dsa_indexer_topk(p, p, p, p, p, ctypes.byref(L2), p, 1, 16, 64, 128, 100, 9000,
+                                p, p, need, None) == UNSUPPORTED              # k too large
+    assert lib.dsa_indexer_topk(p, p, p, p, p, ctypes.byref(L2), p, 1, 16, 16, 128, 100, 32,
+                                p, p, need, None) == UNSUPPORTED              # 16 heads: > 4 rows a tile
