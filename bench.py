@@ -343,6 +343,91 @@ def measure_other_workload(name, dev, steps, warmup, hbm_peak, bf16_peak):
     return res
 
 
+def measure_hisparse(lay, dev, hbm_peak, C=4096, reps=10):
+    """The host-tier working set on the decode batch: the full latent cache in pinned host
+    memory, C device slots per sequence (LRU), the step's own top-k selection.  Times the
+    fetch of a cold step (every selected row comes from the host), of a step whose
+    selection is already resident (all hits) and of one with half the selection new, and
+    the sparse MLA reading the working set against the MLA over the full device cache."""
+    import torch
+    from sparse_attention_29_b300 import capi
+    c = lay.case
+    B, D, Lmax, k = c.B, c.D, c.Lmax, c.k
+    host_kv = c.kv[0].view(torch.int16).cpu().pin_memory()
+    res = torch.empty((B, Lmax), dtype=torch.int32, device=dev)
+    stok = torch.empty((B, C), dtype=torch.int32, device=dev)
+    use = torch.empty((B, C), dtype=torch.int32, device=dev)
+    pool = torch.empty((B * C, D), dtype=torch.int16, device=dev)
+    stats = torch.zeros((B, 2), dtype=torch.int32, device=dev)
+    lay.indexer()
+    lay.topk()
+    idx = lay.idx.clone()
+    # a second selection sharing half of each row (the other half: the rows' next tokens
+    # outside the first selection), still ascending
+    idx2 = idx.clone()
+    for b in range(B):
+        row = idx[b]
+        free = torch.ones(Lmax, dtype=torch.bool, device=dev)
+        free[row[row >= 0].long()] = False
+        free[c.lengths[b]:] = False
+        new = torch.nonzero(free).flatten()[: k // 2].to(torch.int32)
+        idx2[b] = torch.sort(torch.cat([row[: k - new.numel()], new])).values
+    layout = capi.make_layout(B * C, block_table=res, page_size=1)
+    ev = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+
+    def fetch_ms(sel, step):
+        a, e = ev()
+        a.record()
+        capi.dsa_hisparse_fetch(sel, B, k, step, host_kv, c.seq_start, D, res, Lmax, stok, use, C,
+                                pool, stats)
+        e.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(e)
+
+    cold, warm, half = [], [], []
+    step = 0
+    for _ in range(reps):
+        capi.dsa_hisparse_init(res, B, Lmax, stok, use, C)
+        step += 1
+        cold.append(fetch_ms(idx, step))
+        step += 1
+        warm.append(fetch_ms(idx, step))
+        st_warm = stats.sum(0).tolist()
+        step += 1
+        half.append(fetch_ms(idx2, step))
+        st_half = stats.sum(0).tolist()
+    out = torch.empty_like(lay.out[0])
+    lse = torch.empty_like(lay.lse[0])
+
+    def mla_ms(kv, lay_):
+        times = []
+        for _ in range(reps):
+            a, e = ev()
+            a.record()
+            capi.dsa_sparse_mla_decode(c.q[0], kv, lay_, idx2, B, c.H, c.d, c.r, k, c.softmax_scale,
+                                       out, lse, lay.workspace, lay.ws_bytes)
+            e.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(e))
+        return sorted(times)[len(times) // 2]
+
+    mla_pool = mla_ms(pool.view(torch.bfloat16), layout)
+    mla_full = mla_ms(c.kv[0], lay.layout)
+    st, code = capi.dsa_device_error()
+    med = lambda x: sorted(x)[len(x) // 2]  # noqa: E731
+    cold_bytes = B * k * D * 2
+    return {"workload": f"decode_32k with the latent cache in pinned host memory and {C} device "
+                        f"slots per sequence ({C / c.lengths[0]:.3f} of the context), LRU",
+            "fetch_us": {"cold": med(cold) * 1e3, "all_hits": med(warm) * 1e3,
+                         "half_new": med(half) * 1e3},
+            "hits_misses": {"all_hits": st_warm, "half_new": st_half},
+            "host_link_gbs_cold": cold_bytes / (med(cold) * 1e-3) / 1e9,
+            "sparse_mla_us": {"through_working_set": mla_pool * 1e3, "full_device_cache": mla_full * 1e3},
+            "device_bytes": {"working_set": B * C * D * 2, "full_cache": c.n_phys * D * 2},
+            "device_check": "ok" if st == capi.DSA_OK else f"code {code:#x}",
+            "timing": "CUDA events around single launches, median of %d" % reps}
+
+
 def make_workload(name, device, seed_offset=0):
     from sparse_attention_29_b300 import inputs
     return inputs.preset(name, seed=inputs.PRESETS[name]["seed"] + seed_offset, device=device)
@@ -694,7 +779,22 @@ def main():
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(s2.elapsed_time(e2), world, dev) / args.steps
         layers[0].check_device_error()
+        # the host link on its own: one upload and one download of a step's buffers
+        def copy_us(dst, src, n=10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(n):
+                dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n * 1e3
+        up_us = copy_us(packed[0][0], host_in[0])
+        down_us = copy_us(host_out[0], packed[0][1])
         e2e = {"value": job_rate(q_tokens, world, e2e_ms), "unit": UNIT,
+               "host_link": {"h2d_us": up_us, "h2d_gbs": h2d / up_us / 1e3,
+                             "d2h_us": down_us, "d2h_gbs": d2h / down_us / 1e3},
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "host_submit_us_per_step": host_us,
                "pipelined": "one packed upload and one packed download per step (pinned host "
@@ -768,6 +868,10 @@ def main():
             except Exception as exc:
                 others[name] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
         line["other_workloads"] = others
+        try:  # the host-tier working set on the decode batch
+            line["hisparse"] = measure_hisparse(layers[0], dev, hbm_peak)
+        except Exception as exc:
+            line["hisparse"] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
     if cpu_base:
         line["cpu_baseline"] = cpu_base
     if args.profile:

@@ -248,6 +248,45 @@ dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const i
                               const dsa_cache_layout_t *layout, uint8_t *k8_cache,
                               float *k_scale, uint16_t *kv_cache, void *stream);
 
+/*
+ * Host-tier working set of a latent cache (HiSparse, remio.ai: the section on HiSparse).
+ * The full latent history of every sequence stays in pinned host memory; the device keeps
+ * C slots per sequence, managed least recently used, and each decode step makes its
+ * selected tokens resident before the sparse MLA reads them.  The result of the attention
+ * does not change: the MLA reads the same rows through another layout.
+ *   residency  [B, Lmax] int32: the pool row (b*C + slot) holding token t of sequence b,
+ *              or -1.  It is a block table with one-token pages, so the step's MLA reads
+ *              the working set through dsa_cache_layout_t{seq_start = NULL, block_table =
+ *              residency, page_size = 1, pages_per_seq = Lmax, num_rows = B*C} and pool.
+ *   slot_token [B, C] int32: the token in each slot, or -1.
+ *   slot_use   [B, C] uint32: the last step that used each slot (0: never).
+ *   pool       [B*C, D] bf16: the device working set.
+ * dsa_hisparse_init sets residency and slot_token to -1 and slot_use to 0.
+ * dsa_hisparse_fetch, for step `step` (>= 1, increasing from call to call) and the step's
+ * selection idx [B, k] (-1 skipped; a token at most once per row):
+ *   - a resident selected token is a hit: its slot's last use becomes `step`;
+ *   - the others are misses, taken in index-row order; the victims are the slots of the
+ *     sequence not used in this step, least recently used first (the lower slot first
+ *     among equal last uses), listed in ascending slot order; miss i takes victim i: the
+ *     victim's previous token stops being resident, the miss's row (host_kv row
+ *     host_seq_start[b] + t, D bf16 values) is copied into the slot, and its last use
+ *     becomes `step`;
+ *   - stats [B, 2] (nullable) receives (hits, misses) per sequence.
+ * host_kv is a device-accessible address of pinned host memory (cudaHostAlloc with
+ * cudaHostAllocMapped, or any pinned allocation under unified addressing); the missed rows
+ * are read from it directly by the kernel.  Supported: D % 8 == 0, k <= C <= 16384,
+ * k <= 8192; host_kv and pool 16-byte aligned.  Steps out of order (fewer free slots than
+ * misses) set the device error word (kernel id 6) and change nothing.
+ */
+dsa_status_t dsa_hisparse_init(int32_t *residency, int B, int Lmax, int32_t *slot_token,
+                               uint32_t *slot_use, int C, void *stream);
+
+dsa_status_t dsa_hisparse_fetch(const int32_t *idx, int B, int k, uint32_t step,
+                                const uint16_t *host_kv, const int32_t *host_seq_start, int D,
+                                int32_t *residency, int Lmax, int32_t *slot_token,
+                                uint32_t *slot_use, int C, uint16_t *pool, int32_t *stats,
+                                void *stream);
+
 typedef enum {
     DSA_OP_INDEXER = 0,
     DSA_OP_TOPK = 1,
@@ -266,7 +305,7 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
  * Synchronises `stream`, then reads and clears the device error word.  Returns DSA_OK
  * if no device-side check fired since the last call, else DSA_ERR_DEVICE and, if `code`
  * is not NULL, the first recorded code (kernel id << 16 | reason; kernel ids: 1 indexer,
- * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append).
+ * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append, 6 host-tier fetch).
  */
 dsa_status_t dsa_device_error(void *stream, uint32_t *code);
 

@@ -82,6 +82,8 @@ def _load():
         lib.orc_indexer_flops.argtypes = [I, I, D]
         lib.orc_num_threads.restype = I
         lib.orc_num_threads.argtypes = []
+        lib.orc_hisparse_step.restype = I
+        lib.orc_hisparse_step.argtypes = [P, I, ctypes.c_uint32, P, I, P, P, I, P, P]
         _lib = lib
     return _lib
 
@@ -278,3 +280,29 @@ def indexshare_indexer_cut(G):
 
 def indexer_flops(Hi, Di, n_keys):
     return _load().orc_indexer_flops(Hi, Di, float(n_keys))
+
+
+# ---- HiSparse host tier ------------------------------------------------------------------
+
+class HiSparseState:
+    """One sequence's device working set under the oracle's LRU policy (step of the C file):
+    res [Lmax] slot or -1, slot_tok [C] token or -1, slot_use [C] last use (0: never)."""
+
+    def __init__(self, Lmax, C):
+        self.res = np.full(Lmax, -1, np.int32)
+        self.slot_tok = np.full(C, -1, np.int32)
+        self.slot_use = np.zeros(C, np.uint32)
+
+    def step(self, idx_row, step):
+        """Apply one step; returns (hits, [(token, slot) loaded])."""
+        lib = _load()
+        row = np.ascontiguousarray(np.asarray(idx_row, np.int32))
+        k = row.size
+        loaded = np.empty(2 * max(k, 1), np.int32)
+        hits = ctypes.c_int(0)
+        m = lib.orc_hisparse_step(_ptr(row), k, int(step), _ptr(self.res), self.res.size,
+                                  _ptr(self.slot_tok), _ptr(self.slot_use), self.slot_tok.size,
+                                  _ptr(loaded), ctypes.byref(hits))
+        if m < 0:
+            raise ValueError("oracle HiSparse step: index out of range or too few slots")
+        return hits.value, [(int(loaded[2 * i]), int(loaded[2 * i + 1])) for i in range(m)]

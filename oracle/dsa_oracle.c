@@ -501,3 +501,94 @@ int orc_num_threads(void)
     return 1;
 #endif
 }
+
+/* ---------- HiSparse host tier [ES, "HiSparse saca el historial completo de la GPU"] ---- */
+
+/*
+ * One decode step of a sequence's device working set: the full latent history stays in
+ * host memory, the device keeps C slots, managed least recently used.  For the step's
+ * index row idx[0..k-1] (-1 entries skipped; no token twice):
+ *   - a selected token that is resident (res[t] = its slot) is a hit: its slot's last
+ *     use becomes `step`;
+ *   - the other selected tokens are misses, taken in their order in the row;
+ *   - the victims are the m = #misses slots not used in this step (last use < step)
+ *     that were used least recently: smallest last use first, the lower slot first
+ *     among equal ones (never-used slots have last use 0);
+ *   - the i-th miss (row order) goes to the i-th victim (ascending slot order): the
+ *     victim's previous token stops being resident, the miss becomes resident there, the
+ *     slot's last use becomes `step`, and loaded[i] records (token, slot).
+ * res [Lmax] slot or -1, slot_tok [C] token or -1, slot_use [C] last use; step >= 1.
+ * Returns the number of misses, or -1 if there are more misses than free candidates
+ * or an index is out of range.
+ */
+typedef struct {
+    uint32_t use;
+    int32_t slot;
+} lru_t;
+
+static int lru_cmp(const void *a, const void *b)
+{
+    const lru_t *x = a, *y = b;
+    if (x->use != y->use)
+        return x->use < y->use ? -1 : 1;
+    return (x->slot > y->slot) - (x->slot < y->slot);
+}
+
+int orc_hisparse_step(const int32_t *idx, int k, uint32_t step, int32_t *res, int Lmax,
+                      int32_t *slot_tok, uint32_t *slot_use, int C, int32_t *loaded,
+                      int *hits_out)
+{
+    int hits = 0, m = 0;
+    int32_t *miss = malloc(sizeof(int32_t) * (size_t)(k > 0 ? k : 1));
+    for (int j = 0; j < k; ++j) {
+        const int32_t t = idx[j];
+        if (t < 0)
+            continue;
+        if (t >= Lmax) {
+            free(miss);
+            return -1;
+        }
+        if (res[t] >= 0) {
+            slot_use[res[t]] = step;
+            ++hits;
+        } else {
+            miss[m++] = t;
+        }
+    }
+    lru_t *cand = malloc(sizeof(lru_t) * (size_t)C);
+    int nc = 0;
+    for (int s = 0; s < C; ++s)
+        if (slot_use[s] < step) {
+            cand[nc].use = slot_use[s];
+            cand[nc].slot = s;
+            ++nc;
+        }
+    if (m > nc) {
+        free(miss);
+        free(cand);
+        return -1;
+    }
+    qsort(cand, (size_t)nc, sizeof(lru_t), lru_cmp); /* least recently used first */
+    int32_t *victim = malloc(sizeof(int32_t) * (size_t)(m > 0 ? m : 1));
+    for (int i = 0; i < m; ++i)
+        victim[i] = cand[i].slot;
+    qsort(victim, (size_t)m, sizeof(int32_t), int_cmp); /* ascending slot order */
+    for (int i = 0; i < m; ++i) {
+        const int32_t v = victim[i], t = miss[i];
+        if (slot_tok[v] >= 0)
+            res[slot_tok[v]] = -1;
+        res[t] = v;
+        slot_tok[v] = t;
+        slot_use[v] = step;
+        if (loaded) {
+            loaded[2 * i] = t;
+            loaded[2 * i + 1] = v;
+        }
+    }
+    if (hits_out)
+        *hits_out = hits;
+    free(miss);
+    free(cand);
+    free(victim);
+    return m;
+}

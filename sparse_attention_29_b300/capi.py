@@ -26,7 +26,8 @@ DSA_NOALLOC_SCRATCH_BYTES = 20 << 20
 EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
            "dsa_sparse_mla_decode", "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_prefill",
            "dsa_sparse_mla_shared", "dsa_cache_append", "dsa_workspace_bytes",
-           "dsa_device_error", "dsa_indexer_topk", "dsa_indexer_topk_workspace_bytes")
+           "dsa_device_error", "dsa_indexer_topk", "dsa_indexer_topk_workspace_bytes",
+           "dsa_hisparse_init", "dsa_hisparse_fetch")
 
 
 class DsaError(RuntimeError):
@@ -68,6 +69,10 @@ def load(path: str = LIB_PATH):
     lib.dsa_indexer_topk.argtypes = [P, P, P, P, P, LP, P, I, I, I, I, I, I, P, P, S, P]
     lib.dsa_indexer_topk_workspace_bytes.restype = S
     lib.dsa_indexer_topk_workspace_bytes.argtypes = [I, I, I]
+    lib.dsa_hisparse_init.restype = I
+    lib.dsa_hisparse_init.argtypes = [P, I, I, P, P, I, P]
+    lib.dsa_hisparse_fetch.restype = I
+    lib.dsa_hisparse_fetch.argtypes = [P, I, I, ctypes.c_uint32, P, P, I, P, I, P, P, I, P, P, P]
     lib.dsa_sparse_mla_decode.restype = I
     lib.dsa_sparse_mla_decode.argtypes = [P, P, LP, P, I, I, I, I, I, F, P, P, P, S, P]
     lib.dsa_sparse_mla_decode_noalloc.restype = I
@@ -147,6 +152,22 @@ def dsa_indexer_topk_workspace_bytes(B, T, Lmax) -> int:
     if n == ctypes.c_size_t(-1).value:
         raise DsaError("dsa_indexer_topk_workspace_bytes", 1)
     return n
+
+
+def dsa_hisparse_init(residency, B, Lmax, slot_token, slot_use, C, stream=None):
+    st = load().dsa_hisparse_init(_ptr(residency), B, Lmax, _ptr(slot_token), _ptr(slot_use), C,
+                                  _stream(stream))
+    _check("dsa_hisparse_init", st)
+
+
+def dsa_hisparse_fetch(idx, B, k, step, host_kv, host_seq_start, D, residency, Lmax, slot_token,
+                       slot_use, C, pool, stats=None, stream=None):
+    """host_kv: a pinned host tensor (its address is device-accessible under unified
+    addressing) or a device-accessible address."""
+    st = load().dsa_hisparse_fetch(_ptr(idx), B, k, int(step), _ptr(host_kv), _ptr(host_seq_start),
+                                   D, _ptr(residency), Lmax, _ptr(slot_token), _ptr(slot_use), C,
+                                   _ptr(pool), _ptr(stats), _stream(stream))
+    _check("dsa_hisparse_fetch", st)
 
 
 def dsa_cache_append(k_new, c_new, seq, pos, n, B, Di, D, layout, k8_cache, k_scale, kv_cache,

@@ -472,11 +472,60 @@ dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const i
     return from_cuda(launch_cache_append(p, static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status_t dsa_hisparse_init(int32_t *residency, int B, int Lmax, int32_t *slot_token,
+                               uint32_t *slot_use, int C, void *stream) {
+    if (!residency || !slot_token || !slot_use) return DSA_ERR_INVALID_ARG;
+    if (B <= 0 || Lmax <= 0 || C <= 0) return DSA_ERR_INVALID_ARG;
+    if (C > kMaxHiSlots) return DSA_ERR_UNSUPPORTED;
+    return from_cuda(launch_hisparse_init(residency, (int64_t)B * Lmax, slot_token, slot_use,
+                                          (int64_t)B * C, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status_t dsa_hisparse_fetch(const int32_t *idx, int B, int k, uint32_t step,
+                                const uint16_t *host_kv, const int32_t *host_seq_start, int D,
+                                int32_t *residency, int Lmax, int32_t *slot_token,
+                                uint32_t *slot_use, int C, uint16_t *pool, int32_t *stats,
+                                void *stream) {
+    if (!idx || !host_kv || !host_seq_start || !residency || !slot_token || !slot_use || !pool)
+        return DSA_ERR_INVALID_ARG;
+    if (B <= 0 || k <= 0 || Lmax <= 0 || C <= 0 || D <= 0 || step == 0) return DSA_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(host_kv) || !aligned16(pool)) return DSA_ERR_INVALID_ARG;
+    if (k > kMaxHiK || C > kMaxHiSlots) return DSA_ERR_UNSUPPORTED;
+    if (C < k) return DSA_ERR_INVALID_ARG;  // a step's selection must fit the working set
+    if ((int64_t)B * C >= ((int64_t)1 << 31)) return DSA_ERR_UNSUPPORTED;
+    // the kernel reads host_kv directly: it must be pinned host memory mapped at this very
+    // address (or device memory); anything else is refused before a launch could fault
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, host_kv) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DSA_ERR_INVALID_ARG;
+    }
+    const bool mapped_host = pa.type == cudaMemoryTypeHost && pa.devicePointer == host_kv;
+    const bool on_device = pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged;
+    if (!mapped_host && !on_device) return DSA_ERR_INVALID_ARG;
+    HiParams p;
+    p.idx = idx;
+    p.host_kv = host_kv;
+    p.host_seq_start = host_seq_start;
+    p.residency = residency;
+    p.slot_token = slot_token;
+    p.slot_use = slot_use;
+    p.pool = pool;
+    p.stats = stats;
+    p.step = step;
+    p.B = B;
+    p.k = k;
+    p.Lmax = Lmax;
+    p.C = C;
+    p.D = D;
+    return from_cuda(launch_hisparse_fetch(p, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_device_error(void *stream, uint32_t *code) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return from_cuda(cudaErrorUnknown);
-    const uint32_t words[4] = {take_error_indexer(), take_error_topk(), take_error_mla(),
-                               take_error_append()};
+    const uint32_t words[5] = {take_error_indexer(), take_error_topk(), take_error_mla(),
+                               take_error_append(), take_error_hisparse()};
     uint32_t first = 0;
     for (uint32_t v : words) {
         if (v == 0xFFFFFFFFu) return DSA_ERR_CUDA;

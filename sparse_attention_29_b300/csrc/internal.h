@@ -168,6 +168,26 @@ void mla_split_plan(int rows, int k, int num_sms, int d, int *splits, int *tiles
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
 cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);
 
+// ---- host-tier working set (HiSparse) ----------------------------------------------------
+constexpr int kMaxHiSlots = 16384;  // device slots per sequence
+constexpr int kMaxHiK = 8192;       // index-row length
+struct HiParams {
+    const int32_t *idx;             // [B, k] this step's selection (-1 skipped)
+    const uint16_t *host_kv;        // device-accessible pointer to the host cache [rows, D]
+    const int32_t *host_seq_start;  // [B] first host row of each sequence
+    int32_t *residency;             // [B, Lmax] global pool row of each token, or -1
+    int32_t *slot_token;            // [B, C] token in each slot, or -1
+    uint32_t *slot_use;             // [B, C] last step each slot was used (0: never)
+    uint16_t *pool;                 // [B * C, D] device working set
+    int32_t *stats;                 // [B, 2] hits, misses (nullable)
+    uint32_t step;
+    int B, k, Lmax, C, D;
+};
+cudaError_t launch_hisparse_fetch(const HiParams &p, cudaStream_t stream);
+cudaError_t launch_hisparse_init(int32_t *residency, int64_t n_res, int32_t *slot_token,
+                                 uint32_t *slot_use, int64_t n_slots, cudaStream_t stream);
+uint32_t take_error_hisparse();
+
 // ---- cache append: new tokens' indexer keys (quantised) and latent rows into the caches
 struct AppendParams {
     const float *k_new;     // [n, Di] fp32

@@ -116,3 +116,22 @@ def test_fused_indexer_topk_checks_fail_before_any_launch(lib):
                                 p, p, need, None) == UNSUPPORTED              # k too large
     assert lib.dsa_indexer_topk(p, p, p, p, p, ctypes.byref(L2), p, 1, 16, 16, 128, 100, 32,
                                 p, p, need, None) == UNSUPPORTED              # 16 heads: > 4 rows a tile
+
+
+def test_hisparse_checks_fail_before_any_launch(lib):
+    INVALID, UNSUPPORTED = 1, 2
+    p = 0x1000
+    U32 = ctypes.c_uint32
+    # null arguments, step 0, a working set smaller than the selection, sizes past the build
+    assert lib.dsa_hisparse_fetch(None, 1, 8, U32(1), p, p, 576, p, 100, p, p, 16, p, None,
+                                  None) == INVALID
+    assert lib.dsa_hisparse_fetch(p, 1, 8, U32(0), p, p, 576, p, 100, p, p, 16, p, None,
+                                  None) == INVALID
+    assert lib.dsa_hisparse_fetch(p, 1, 32, U32(1), p, p, 576, p, 100, p, p, 16, p, None,
+                                  None) == INVALID
+    assert lib.dsa_hisparse_fetch(p, 1, 8, U32(1), p, p, 570, p, 100, p, p, 16, p, None,
+                                  None) == INVALID                         # D % 8 != 0
+    assert lib.dsa_hisparse_fetch(p, 1, 9000, U32(1), p, p, 576, p, 100000, p, p, 9000, p,
+                                  None, None) == UNSUPPORTED
+    assert lib.dsa_hisparse_init(p, 1, 100, p, p, 20000, None) == UNSUPPORTED
+    assert lib.dsa_hisparse_init(None, 1, 100, p, p, 16, None) == INVALID

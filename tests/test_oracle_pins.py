@@ -459,3 +459,45 @@ def test_cache_append_codes_round_the_exact_quotient_once():
             twice = oracle.e4m3_encode(np.float32(k[i, c]) / ks[i])
             differs += int(twice != want)
     assert differs >= 3 * 6  # the planted keys do separate the two readings
+
+
+def test_hisparse_lru_hand_worked_example(golden):
+    g = golden("hisparse_lru.txt")
+    st = oracle.HiSparseState(int(g["Lmax"]), int(g["C"]))
+    hits = []
+    for s in (1, 2, 3):
+        row = np.atleast_1d(np.asarray(g[f"step{s}"], dtype=np.int32))
+        h, loaded = st.step(row, s)
+        hits.append(h)
+        want = np.atleast_1d(np.asarray(g[f"loaded{s}"], dtype=np.int64)).reshape(-1, 2)
+        assert loaded == [tuple(x) for x in want.tolist()], s
+    assert hits == [int(x) for x in g["hits"]]
+    assert st.res.tolist() == [int(x) for x in g["final_residency"]]
+    assert st.slot_tok.tolist() == [int(x) for x in g["final_slot_token"]]
+    assert st.slot_use.tolist() == [int(x) for x in g["final_slot_use"]]
+
+
+def test_hisparse_policy_invariants():
+    """Over random steps: every selected token is resident afterwards, residency and slot
+    tokens stay inverse maps, the set of evicted tokens were never used later than any
+    non-selected resident token that stayed, and the hit count is the overlap with the
+    tokens resident before the step."""
+    rng = np.random.default_rng(5)
+    Lmax, C, k = 300, 40, 25
+    st = oracle.HiSparseState(Lmax, C)
+    for step in range(1, 30):
+        sel = np.sort(rng.choice(Lmax if step % 3 else 60, size=k, replace=False)).astype(np.int32)
+        before = {int(t): int(st.res[t]) for t in np.nonzero(st.res >= 0)[0]}
+        use_before = st.slot_use.copy()
+        hits, loaded = st.step(sel, step)
+        assert hits == sum(int(t) in before for t in sel)
+        assert all(st.res[t] >= 0 for t in sel)
+        for s, t in enumerate(st.slot_tok):
+            if t >= 0:
+                assert st.res[t] == s
+        assert int((st.res >= 0).sum()) == int((st.slot_tok >= 0).sum()) <= C
+        victims = {v for _, v in loaded}
+        kept = [s for s in range(C) if s not in victims and use_before[s] < step
+                and st.slot_use[s] < step]
+        if victims and kept:
+            assert max(use_before[v] for v in victims) <= min(use_before[s] for s in kept)
