@@ -82,6 +82,8 @@ def _load():
         lib.orc_indexer_flops.argtypes = [I, I, D]
         lib.orc_num_threads.restype = I
         lib.orc_num_threads.argtypes = []
+        lib.orc_sparse_mha.restype = I
+        lib.orc_sparse_mha.argtypes = [P, P, P, P, P, P, I, I, P, I, I, I, I, I, I, I, I, D, P, P]
         lib.orc_hisparse_step.restype = I
         lib.orc_hisparse_step.argtypes = [P, I, ctypes.c_uint32, P, I, P, P, I, P, P]
         _lib = lib
@@ -216,6 +218,28 @@ def sparse_mla(case, idx, layer=0, check_causal=True):
                             float(case.softmax_scale), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle sparse MLA: bad argument or index outside the causal window")
+    return out, lse
+
+
+def sparse_mha(case, idx, w_uk, w_uv, q_mha, layer=0):
+    """(out [rows, H, vd] float64, lse [rows, H]) of MLA in MHA mode (step of the C file):
+    w_uk [H, dn, d] and w_uv [H, vd, d] bf16 up-projections, q_mha [rows, H, dn + r] bf16."""
+    lib = _load()
+    seq_start, bt, ps, pps = _addressing(case)
+    wk = _np(w_uk, np.uint16)
+    wv = _np(w_uv, np.uint16)
+    H, dn, d = wk.shape
+    vd = wv.shape[1]
+    ix = _np(idx, np.int32)
+    rows = case.B * case.T
+    out = np.empty((rows, H, vd), dtype=np.float64)
+    lse = np.empty((rows, H), dtype=np.float64)
+    rc = lib.orc_sparse_mha(_ptr(_np(q_mha, np.uint16)), _ptr(_np(case.kv[layer], np.uint16)),
+                            _ptr(wk), _ptr(wv), _ptr(seq_start), _ptr(bt), ps, pps, _ptr(ix),
+                            case.B, case.T, H, d, case.r, dn, vd, ix.shape[1],
+                            float(case.softmax_scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle sparse MHA: bad argument")
     return out, lse
 
 

@@ -592,3 +592,92 @@ int orc_hisparse_step(const int32_t *idx, int k, uint32_t step, int32_t *res, in
     free(victim);
     return m;
 }
+
+/* ---------- MLA in MHA mode [GLM53 §Sparse MLA: MLA's two modes] --------------------- */
+
+/*
+ * MHA mode: the latent row c_j (d = 512 latent dims, then r = 64 rope dims) is projected up
+ * per head h into a key of dn "nope" dims, w_uk[h] . c_j[:d], followed by the shared rope
+ * dims c_j[d:d+r], and a value of vd dims, w_uv[h] . c_j[:d]; each query row t and head h
+ * attends over the valid entries j of idx[t, :] with its own query q[t,h,:] (dn + r):
+ *   logit_j = scale * (q[t,h,:dn] . (w_uk[h] c_j[:d]) + q[t,h,dn:] . c_j[d:d+r])
+ *   o[t,h,:] = sum_j softmax(logit)_j (w_uv[h] c_j[:d])            (vd values)
+ * w_uk [H, dn, d], w_uv [H, vd, d], q [rows, H, dn + r], all bf16 codes; no intermediate
+ * value is rounded.  With w_uk folded into the query (the absorbed query w_uk[h]^T q_nope)
+ * this is the MQA form of step 3 followed by w_uv: the two modes compute one attention.
+ * Returns 0, or -1 on a bad argument.
+ */
+int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, const uint16_t *w_uk,
+                   const uint16_t *w_uv, const int32_t *seq_start, const int32_t *block_table,
+                   int page_size, int pages_per_seq, const int32_t *idx, int B, int T, int H,
+                   int d, int r, int dn, int vd, int K, double scale, double *out, double *lse)
+{
+    if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || r < 0 || dn <= 0 || vd <= 0 || K <= 0 ||
+        d > 1024)
+        return -1;
+    const int D = d + r, dq = dn + r;
+    const int rows = B * T;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int th = 0; th < rows * H; ++th) {
+        const int t = th / H, h = th % H, b = t / T;
+        const int32_t *sel = idx + (int64_t)t * K;
+        const uint16_t *qh = q + ((int64_t)t * H + h) * dq;
+        double *o = out + ((int64_t)t * H + h) * vd;
+        double *logit = malloc(sizeof(double) * (size_t)K);
+        double *vrow = malloc(sizeof(double) * (size_t)vd);
+        double c[1024];
+        double m = -INFINITY;
+        for (int e = 0; e < vd; ++e)
+            o[e] = 0.0;
+        for (int j = 0; j < K; ++j) {
+            logit[j] = -INFINITY;
+            if (sel[j] < 0)
+                continue;
+            const int64_t row = phys_row(b, sel[j], seq_start, block_table, page_size,
+                                         pages_per_seq);
+            for (int e = 0; e < d; ++e)
+                c[e] = orc_bf16_to_double(kv[row * D + e]);
+            double dot = 0.0;
+            for (int i = 0; i < dn; ++i) {
+                double k_i = 0.0; /* the up-projected key's nope dim i */
+                for (int e = 0; e < d; ++e)
+                    k_i += orc_bf16_to_double(w_uk[((int64_t)h * dn + i) * d + e]) * c[e];
+                dot += orc_bf16_to_double(qh[i]) * k_i;
+            }
+            for (int i = 0; i < r; ++i)
+                dot += orc_bf16_to_double(qh[dn + i]) * orc_bf16_to_double(kv[row * D + d + i]);
+            logit[j] = scale * dot;
+            if (logit[j] > m)
+                m = logit[j];
+        }
+        double l = 0.0;
+        if (m > -INFINITY) {
+            for (int j = 0; j < K; ++j) {
+                if (sel[j] < 0)
+                    continue;
+                const int64_t row = phys_row(b, sel[j], seq_start, block_table, page_size,
+                                             pages_per_seq);
+                const double pj = exp(logit[j] - m);
+                l += pj;
+                for (int e = 0; e < d; ++e)
+                    c[e] = orc_bf16_to_double(kv[row * D + e]);
+                for (int i = 0; i < vd; ++i) {
+                    double v_i = 0.0; /* the up-projected value's dim i */
+                    for (int e = 0; e < d; ++e)
+                        v_i += orc_bf16_to_double(w_uv[((int64_t)h * vd + i) * d + e]) * c[e];
+                    vrow[i] = v_i;
+                }
+                for (int i = 0; i < vd; ++i)
+                    o[i] += pj * vrow[i];
+            }
+            for (int i = 0; i < vd; ++i)
+                o[i] /= l;
+            lse[(int64_t)t * H + h] = m + log(l);
+        } else {
+            lse[(int64_t)t * H + h] = -INFINITY;
+        }
+        free(logit);
+        free(vrow);
+    }
+    return 0;
+}

@@ -501,3 +501,50 @@ def test_hisparse_policy_invariants():
                 and st.slot_use[s] < step]
         if victims and kept:
             assert max(use_before[v] for v in victims) <= min(use_before[s] for s in kept)
+
+
+def _mha_inputs(seed, H, d, r, dn, vd, lengths, T, k):
+    """Integer-valued weights and queries: with w_uk and q_nope in {-1, 0, 1} the absorbed
+    query w_uk[h]^T q_nope is an integer of magnitude <= dn, exact in bf16."""
+    case = inputs.make_case(kind="int", seed=seed, lengths=lengths, T=T, Hi=4, Di=32, H=H, d=d,
+                            r=r, k=k, softmax_scale=1.0 / 8.0)
+    g = torch.Generator().manual_seed(seed)
+    w_uk = torch.randint(-1, 2, (H, dn, d), generator=g).to(torch.bfloat16)
+    w_uv = torch.randint(-2, 3, (H, vd, d), generator=g).to(torch.bfloat16)
+    q_nope = torch.randint(-1, 2, (case.rows, H, dn), generator=g).float()
+    q_rope = case.q[0][:, :, d:].float()
+    q_mha = torch.cat([q_nope, q_rope], dim=2).to(torch.bfloat16)
+    q_abs = torch.einsum("hie,thi->the", w_uk.float(), q_nope)
+    assert torch.equal(q_abs.to(torch.bfloat16).float(), q_abs)  # exact in bf16
+    case.q = [torch.cat([q_abs, q_rope], dim=2).to(torch.bfloat16)]
+    return case, w_uk, w_uv, q_mha
+
+
+def test_mha_mode_equals_absorbed_mqa_then_value_projection():
+    """MLA's MHA and MQA modes compute one attention [GLM53 §Sparse MLA]: the MHA-mode oracle
+    equals the (independently pinned) MQA oracle fed the absorbed query, followed by the
+    value up-projection, to fp64 round-off -- for sparse index sets with -1 holes."""
+    H, d, r, dn, vd, k = 3, 64, 16, 32, 48, 24
+    case, w_uk, w_uv, q_mha = _mha_inputs(11, H, d, r, dn, vd, [50, 37], 3, k)
+    rng = np.random.default_rng(3)
+    idx = np.full((case.rows, k), -1, np.int32)
+    for t in range(case.rows):
+        n = int(case.q_pos[t]) + 1
+        m = min(n, k - 3)
+        idx[t, :m] = np.sort(rng.choice(n, size=m, replace=False))
+    o_lat, lse_mqa = oracle.sparse_mla(case, idx)
+    want = np.einsum("hve,the->thv", w_uv.double().numpy(), o_lat)
+    got, lse_mha = oracle.sparse_mha(case, idx, w_uk, w_uv, q_mha)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-9 * np.abs(want).max())
+    np.testing.assert_allclose(lse_mha, lse_mqa, rtol=1e-13, atol=1e-12)
+
+
+def test_mha_mode_one_selected_token_gives_its_value():
+    H, d, r, dn, vd, k = 2, 64, 16, 32, 32, 8
+    case, w_uk, w_uv, q_mha = _mha_inputs(12, H, d, r, dn, vd, [20], 1, k)
+    idx = np.full((1, k), -1, np.int32)
+    idx[0, 3] = 7
+    got, lse = oracle.sparse_mha(case, idx, w_uk, w_uv, q_mha)
+    c = case.kv[0][int(case.seq_start[0]) + 7, :d].double().numpy()
+    want = np.einsum("hve,e->hv", w_uv.double().numpy(), c)
+    np.testing.assert_array_equal(got[0], want)
