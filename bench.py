@@ -428,8 +428,13 @@ def measure_hisparse(lay, dev, hbm_peak, C=4096, reps=10):
             "timing": "CUDA events around single launches, median of %d" % reps}
 
 
-def make_workload(name, device, seed_offset=0):
+def make_workload(name, device, seed_offset=0, rows=0):
     from sparse_attention_29_b300 import inputs
+    if rows and inputs.PRESETS[name]["T"] > 1:
+        p = dict(inputs.PRESETS[name])
+        p["seed"] += seed_offset
+        p["T"] = rows
+        return inputs.make_case(name, device=device, **p)
     return inputs.preset(name, seed=inputs.PRESETS[name]["seed"] + seed_offset, device=device)
 
 
@@ -578,6 +583,11 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="lean run for profiler captures: one input set, no clock pre-roll, "
                          "no per-kernel loops, graph replay, e2e or CPU baseline")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="prefill workloads: query rows per sequence (the last ROWS positions; "
+                         "a smaller case of the same kernel, e.g. for profiler captures)")
+    ap.add_argument("--fused", action="store_true",
+                    help="prefill workloads: the step uses the fused indexer + top-k")
     ap.add_argument("--append-only", action="store_true",
                     help="only the cache-append measurement (one JSON object; for profiler "
                          "captures of that kernel)")
@@ -613,7 +623,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_base = cpu_baseline(args.workload)
 
-    sets = [make_workload(args.workload, dev, seed_offset=1000 * rank + 17 * i)
+    sets = [make_workload(args.workload, dev, seed_offset=1000 * rank + 17 * i, rows=args.rows)
             for i in range(args.sets)]
     layers = [DsaLayer(c) for c in sets]
     # every set's per-query inputs and outputs as views of one device buffer each (the
@@ -626,6 +636,8 @@ def main():
     def step(lay):
         if shared:
             lay.run_shared()
+        elif args.fused and case.T > 1:
+            lay.run_fused()
         else:
             lay.run()
 

@@ -249,6 +249,45 @@ dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const i
                               float *k_scale, uint16_t *kv_cache, void *stream);
 
 /*
+ * MLA in MHA mode for short contexts (§Sparse MLA: MLA's MHA mode has fewer FLOPs and much
+ * more memory than its MQA mode, and below a context-length threshold it is the faster
+ * one; vLLM uses it from 2K up to about 5K tokens with data-parallel attention).  For head
+ * h and a cached latent row c (d latent dims, then r rope dims):
+ *   key_h = [w_uk[h] . c[:d] (dn dims), c[d:d+r]],   value_h = w_uv[h] . c[:d] (vd dims).
+ *
+ * dsa_mla_up_project: out[i, :] = w . latent[i, :d] for the n rows of `latent` ([n, ld]
+ * bf16, row pitch ld >= d elements), w [N, d] bf16 (w_uk as [H*dn, d], or w_uv as
+ * [H*vd, d]), out [n, N] bf16 (fp32 accumulation, rounded to nearest even).  These are the
+ * per-head keys and values of MHA mode, the memory its cache takes.
+ * Supported: d % 64 == 0, N % 128 == 0, ld % 8 == 0; pointers 16-byte aligned.
+ *
+ * dsa_sparse_mha_prefill: for query row t (rows grouped by sequence as everywhere) and
+ * head h, over the tokens of idx[t, :] (-1 skipped), with q [B*T, H, dn + r] bf16:
+ *   logit_j = scale * q[t,h,:] . key_h(j),   out[t,h,:] = sum_j softmax(logit)_j value_h(j)
+ * (bf16, vd values), lse[t,h] as in dsa_sparse_mla_decode (lse may be NULL).  k_up
+ * [num_rows, H*dn] and v_up [num_rows, H*vd] are dsa_mla_up_project's outputs for the
+ * rows of kv_cache [num_rows, d + r] (the rope dims are read from kv_cache); q_pos [B*T]
+ * bounds the keys each row's tile visits.  The cache is contiguous (layout->seq_start;
+ * no block table).  The selection is applied as a mask over dense 128-key tiles: at these
+ * context lengths it covers much of the context.
+ * workspace: dsa_mha_workspace_bytes(B, T, Lmax) bytes (selection bitmaps), 16-byte aligned.
+ * Supported: dn % 64 == 0, r % 64 == 0, dn + r <= 256, vd in {128, 256}, d % 64 == 0,
+ * Lmax <= 65536, k <= 8192; pointers 16-byte aligned.
+ */
+dsa_status_t dsa_mla_up_project(const uint16_t *latent, int64_t n, int ld, int d,
+                                const uint16_t *w, int N, uint16_t *out, void *stream);
+
+size_t dsa_mha_workspace_bytes(int B, int T, int Lmax);
+
+dsa_status_t dsa_sparse_mha_prefill(const uint16_t *q, const uint16_t *k_up,
+                                    const uint16_t *v_up, const uint16_t *kv_cache,
+                                    const dsa_cache_layout_t *layout, const int32_t *idx,
+                                    const int32_t *q_pos, int B, int T, int H, int d, int r,
+                                    int dn, int vd, int k, int Lmax, float scale, uint16_t *out,
+                                    float *lse, void *workspace, size_t workspace_bytes,
+                                    void *stream);
+
+/*
  * Host-tier working set of a latent cache (HiSparse, remio.ai: the section on HiSparse).
  * The full latent history of every sequence stays in pinned host memory; the device keeps
  * C slots per sequence, managed least recently used, and each decode step makes its
@@ -305,7 +344,7 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
  * Synchronises `stream`, then reads and clears the device error word.  Returns DSA_OK
  * if no device-side check fired since the last call, else DSA_ERR_DEVICE and, if `code`
  * is not NULL, the first recorded code (kernel id << 16 | reason; kernel ids: 1 indexer,
- * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append, 6 host-tier fetch).
+ * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append, 6 host-tier fetch, 7 MHA mode).
  */
 dsa_status_t dsa_device_error(void *stream, uint32_t *code);
 

@@ -83,7 +83,7 @@ def _load():
         lib.orc_num_threads.restype = I
         lib.orc_num_threads.argtypes = []
         lib.orc_sparse_mha.restype = I
-        lib.orc_sparse_mha.argtypes = [P, P, P, P, P, P, I, I, P, I, I, I, I, I, I, I, I, D, P, P]
+        lib.orc_sparse_mha.argtypes = [P, P, ctypes.c_int64, P, P, P, P, I, I, P, I, I, I, I, I, I, I, I, D, P, P]
         lib.orc_hisparse_step.restype = I
         lib.orc_hisparse_step.argtypes = [P, I, ctypes.c_uint32, P, I, P, P, I, P, P]
         _lib = lib
@@ -234,7 +234,8 @@ def sparse_mha(case, idx, w_uk, w_uv, q_mha, layer=0):
     rows = case.B * case.T
     out = np.empty((rows, H, vd), dtype=np.float64)
     lse = np.empty((rows, H), dtype=np.float64)
-    rc = lib.orc_sparse_mha(_ptr(_np(q_mha, np.uint16)), _ptr(_np(case.kv[layer], np.uint16)),
+    kv = _np(case.kv[layer], np.uint16)
+    rc = lib.orc_sparse_mha(_ptr(_np(q_mha, np.uint16)), _ptr(kv), kv.shape[0],
                             _ptr(wk), _ptr(wv), _ptr(seq_start), _ptr(bt), ps, pps, _ptr(ix),
                             case.B, case.T, H, d, case.r, dn, vd, ix.shape[1],
                             float(case.softmax_scale), _ptr(out), _ptr(lse))

@@ -603,20 +603,49 @@ int orc_hisparse_step(const int32_t *idx, int k, uint32_t step, int32_t *res, in
  *   logit_j = scale * (q[t,h,:dn] . (w_uk[h] c_j[:d]) + q[t,h,dn:] . c_j[d:d+r])
  *   o[t,h,:] = sum_j softmax(logit)_j (w_uv[h] c_j[:d])            (vd values)
  * w_uk [H, dn, d], w_uv [H, vd, d], q [rows, H, dn + r], all bf16 codes; no intermediate
- * value is rounded.  With w_uk folded into the query (the absorbed query w_uk[h]^T q_nope)
+ * value is rounded.  The n_rows cached rows are projected up first (per head), then each
+ * row and head attends.  With w_uk folded into the query (the absorbed query w_uk[h]^T q_nope)
  * this is the MQA form of step 3 followed by w_uv: the two modes compute one attention.
  * Returns 0, or -1 on a bad argument.
  */
-int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, const uint16_t *w_uk,
+int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, int64_t n_rows, const uint16_t *w_uk,
                    const uint16_t *w_uv, const int32_t *seq_start, const int32_t *block_table,
                    int page_size, int pages_per_seq, const int32_t *idx, int B, int T, int H,
                    int d, int r, int dn, int vd, int K, double scale, double *out, double *lse)
 {
     if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || r < 0 || dn <= 0 || vd <= 0 || K <= 0 ||
-        d > 1024)
+        n_rows <= 0)
         return -1;
     const int D = d + r, dq = dn + r;
     const int rows = B * T;
+    /* 1. every cached row projected up, per head: kn[h][row] (dn), vv[h][row] (vd) */
+    double *kn = malloc(sizeof(double) * (size_t)H * n_rows * dn);
+    double *vv = malloc(sizeof(double) * (size_t)H * n_rows * vd);
+    if (!kn || !vv) {
+        free(kn);
+        free(vv);
+        return -1;
+    }
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t hr = 0; hr < (int64_t)H * n_rows; ++hr) {
+        const int h = (int)(hr / n_rows);
+        const int64_t row = hr % n_rows;
+        for (int i = 0; i < dn; ++i) {
+            double acc = 0.0;
+            for (int e = 0; e < d; ++e)
+                acc += orc_bf16_to_double(w_uk[((int64_t)h * dn + i) * d + e]) *
+                       orc_bf16_to_double(kv[row * D + e]);
+            kn[hr * dn + i] = acc;
+        }
+        for (int i = 0; i < vd; ++i) {
+            double acc = 0.0;
+            for (int e = 0; e < d; ++e)
+                acc += orc_bf16_to_double(w_uv[((int64_t)h * vd + i) * d + e]) *
+                       orc_bf16_to_double(kv[row * D + e]);
+            vv[hr * vd + i] = acc;
+        }
+    }
+    /* 2. attention per query row and head over the selected tokens */
 #pragma omp parallel for schedule(dynamic, 1)
     for (int th = 0; th < rows * H; ++th) {
         const int t = th / H, h = th % H, b = t / T;
@@ -624,8 +653,6 @@ int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, const uint16_t *w_uk,
         const uint16_t *qh = q + ((int64_t)t * H + h) * dq;
         double *o = out + ((int64_t)t * H + h) * vd;
         double *logit = malloc(sizeof(double) * (size_t)K);
-        double *vrow = malloc(sizeof(double) * (size_t)vd);
-        double c[1024];
         double m = -INFINITY;
         for (int e = 0; e < vd; ++e)
             o[e] = 0.0;
@@ -635,15 +662,10 @@ int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, const uint16_t *w_uk,
                 continue;
             const int64_t row = phys_row(b, sel[j], seq_start, block_table, page_size,
                                          pages_per_seq);
-            for (int e = 0; e < d; ++e)
-                c[e] = orc_bf16_to_double(kv[row * D + e]);
+            const double *kr = kn + ((int64_t)h * n_rows + row) * dn;
             double dot = 0.0;
-            for (int i = 0; i < dn; ++i) {
-                double k_i = 0.0; /* the up-projected key's nope dim i */
-                for (int e = 0; e < d; ++e)
-                    k_i += orc_bf16_to_double(w_uk[((int64_t)h * dn + i) * d + e]) * c[e];
-                dot += orc_bf16_to_double(qh[i]) * k_i;
-            }
+            for (int i = 0; i < dn; ++i)
+                dot += orc_bf16_to_double(qh[i]) * kr[i];
             for (int i = 0; i < r; ++i)
                 dot += orc_bf16_to_double(qh[dn + i]) * orc_bf16_to_double(kv[row * D + d + i]);
             logit[j] = scale * dot;
@@ -658,17 +680,10 @@ int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, const uint16_t *w_uk,
                 const int64_t row = phys_row(b, sel[j], seq_start, block_table, page_size,
                                              pages_per_seq);
                 const double pj = exp(logit[j] - m);
+                const double *vr = vv + ((int64_t)h * n_rows + row) * vd;
                 l += pj;
-                for (int e = 0; e < d; ++e)
-                    c[e] = orc_bf16_to_double(kv[row * D + e]);
-                for (int i = 0; i < vd; ++i) {
-                    double v_i = 0.0; /* the up-projected value's dim i */
-                    for (int e = 0; e < d; ++e)
-                        v_i += orc_bf16_to_double(w_uv[((int64_t)h * vd + i) * d + e]) * c[e];
-                    vrow[i] = v_i;
-                }
                 for (int i = 0; i < vd; ++i)
-                    o[i] += pj * vrow[i];
+                    o[i] += pj * vr[i];
             }
             for (int i = 0; i < vd; ++i)
                 o[i] /= l;
@@ -677,7 +692,8 @@ int orc_sparse_mha(const uint16_t *q, const uint16_t *kv, const uint16_t *w_uk,
             lse[(int64_t)t * H + h] = -INFINITY;
         }
         free(logit);
-        free(vrow);
     }
+    free(kn);
+    free(vv);
     return 0;
 }

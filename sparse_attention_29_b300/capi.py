@@ -27,7 +27,8 @@ EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
            "dsa_sparse_mla_decode", "dsa_sparse_mla_decode_noalloc", "dsa_sparse_mla_prefill",
            "dsa_sparse_mla_shared", "dsa_cache_append", "dsa_workspace_bytes",
            "dsa_device_error", "dsa_indexer_topk", "dsa_indexer_topk_workspace_bytes",
-           "dsa_hisparse_init", "dsa_hisparse_fetch")
+           "dsa_hisparse_init", "dsa_hisparse_fetch", "dsa_mla_up_project",
+           "dsa_mha_workspace_bytes", "dsa_sparse_mha_prefill")
 
 
 class DsaError(RuntimeError):
@@ -69,6 +70,13 @@ def load(path: str = LIB_PATH):
     lib.dsa_indexer_topk.argtypes = [P, P, P, P, P, LP, P, I, I, I, I, I, I, P, P, S, P]
     lib.dsa_indexer_topk_workspace_bytes.restype = S
     lib.dsa_indexer_topk_workspace_bytes.argtypes = [I, I, I]
+    lib.dsa_mla_up_project.restype = I
+    lib.dsa_mla_up_project.argtypes = [P, ctypes.c_int64, I, I, P, I, P, P]
+    lib.dsa_mha_workspace_bytes.restype = S
+    lib.dsa_mha_workspace_bytes.argtypes = [I, I, I]
+    lib.dsa_sparse_mha_prefill.restype = I
+    lib.dsa_sparse_mha_prefill.argtypes = [P, P, P, P, LP, P, P, I, I, I, I, I, I, I, I, I, F, P,
+                                           P, P, S, P]
     lib.dsa_hisparse_init.restype = I
     lib.dsa_hisparse_init.argtypes = [P, I, I, P, P, I, P]
     lib.dsa_hisparse_fetch.restype = I
@@ -152,6 +160,28 @@ def dsa_indexer_topk_workspace_bytes(B, T, Lmax) -> int:
     if n == ctypes.c_size_t(-1).value:
         raise DsaError("dsa_indexer_topk_workspace_bytes", 1)
     return n
+
+
+def dsa_mla_up_project(latent, n, ld, d, w, N, out, stream=None):
+    st = load().dsa_mla_up_project(_ptr(latent), int(n), ld, d, _ptr(w), N, _ptr(out),
+                                   _stream(stream))
+    _check("dsa_mla_up_project", st)
+
+
+def dsa_mha_workspace_bytes(B, T, Lmax) -> int:
+    n = load().dsa_mha_workspace_bytes(B, T, Lmax)
+    if n == ctypes.c_size_t(-1).value:
+        raise DsaError("dsa_mha_workspace_bytes", 1)
+    return n
+
+
+def dsa_sparse_mha_prefill(q, k_up, v_up, kv_cache, layout, idx, q_pos, B, T, H, d, r, dn, vd, k,
+                           Lmax, scale, out, lse, workspace, workspace_bytes, stream=None):
+    st = load().dsa_sparse_mha_prefill(_ptr(q), _ptr(k_up), _ptr(v_up), _ptr(kv_cache),
+                                       ctypes.byref(layout), _ptr(idx), _ptr(q_pos), B, T, H, d, r,
+                                       dn, vd, k, Lmax, float(scale), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check("dsa_sparse_mha_prefill", st)
 
 
 def dsa_hisparse_init(residency, B, Lmax, slot_token, slot_use, C, stream=None):

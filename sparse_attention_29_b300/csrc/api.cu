@@ -521,11 +521,93 @@ dsa_status_t dsa_hisparse_fetch(const int32_t *idx, int B, int k, uint32_t step,
     return from_cuda(launch_hisparse_fetch(p, static_cast<cudaStream_t>(stream)));
 }
 
+static bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_tiled();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+dsa_status_t dsa_mla_up_project(const uint16_t *latent, int64_t n, int ld, int d,
+                                const uint16_t *w, int N, uint16_t *out, void *stream) {
+    if (!latent || !w || !out) return DSA_ERR_INVALID_ARG;
+    if (n <= 0 || ld <= 0 || d <= 0 || N <= 0 || d > ld) return DSA_ERR_INVALID_ARG;
+    if (d % 64 != 0 || N % 128 != 0 || ld % 8 != 0) return DSA_ERR_UNSUPPORTED;
+    if (n >= ((int64_t)1 << 31) - 128 || (int64_t)N * 2 >= ((int64_t)1 << 31)) return DSA_ERR_UNSUPPORTED;
+    if (!aligned16(latent) || !aligned16(w) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+    CUtensorMap xmap, wmap;
+    if (!encode_bf16_2d(&xmap, latent, (uint64_t)ld, (uint64_t)n) ||
+        !encode_bf16_2d(&wmap, w, (uint64_t)d, (uint64_t)N))
+        return DSA_ERR_CUDA;
+    return from_cuda(launch_upproj(xmap, wmap, out, (int)n, N, d, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_mha_workspace_bytes(int B, int T, int Lmax) {
+    if (B <= 0 || T <= 0 || Lmax <= 0) return (size_t)-1;
+    return (size_t)B * T * (size_t)((Lmax + 127) / 128 * 4) * 4;
+}
+
+dsa_status_t dsa_sparse_mha_prefill(const uint16_t *q, const uint16_t *k_up,
+                                    const uint16_t *v_up, const uint16_t *kv_cache,
+                                    const dsa_cache_layout_t *layout, const int32_t *idx,
+                                    const int32_t *q_pos, int B, int T, int H, int d, int r,
+                                    int dn, int vd, int k, int Lmax, float scale, uint16_t *out,
+                                    float *lse, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (!q || !k_up || !v_up || !kv_cache || !layout || !idx || !q_pos || !out || !workspace)
+        return DSA_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || r <= 0 || dn <= 0 || vd <= 0 || k <= 0 || Lmax <= 0)
+        return DSA_ERR_INVALID_ARG;
+    if (!(scale > 0.f)) return DSA_ERR_INVALID_ARG;
+    if (layout->block_table || !layout->seq_start || layout->num_rows <= 0) return DSA_ERR_UNSUPPORTED;
+    if (dn % 64 != 0 || r % 64 != 0 || dn + r > 256 || (vd != 128 && vd != 256) || d % 64 != 0)
+        return DSA_ERR_UNSUPPORTED;
+    if (Lmax > 65536 || k > 8192) return DSA_ERR_UNSUPPORTED;
+    if ((int64_t)B * T >= ((int64_t)1 << 30) || layout->num_rows >= ((int64_t)1 << 31) - 128)
+        return DSA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_up) || !aligned16(v_up) || !aligned16(kv_cache) ||
+        !aligned16(out) || !aligned16(workspace))
+        return DSA_ERR_INVALID_ARG;
+    const size_t need = dsa_mha_workspace_bytes(B, T, Lmax);
+    if (workspace_bytes < need) return DSA_ERR_WORKSPACE;
+    MhaParams p;
+    p.q_pos = q_pos;
+    p.seq_start = layout->seq_start;
+    p.bitmap = static_cast<uint32_t *>(workspace);
+    p.out = out;
+    p.lse = lse;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.d = d;
+    p.r = r;
+    p.dn = dn;
+    p.dq = dn + r;
+    p.vd = vd;
+    p.k = k;
+    p.Lmax = Lmax;
+    p.words = (Lmax + 127) / 128 * 4;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const int64_t nr = layout->num_rows;
+    CUtensorMap qmap, kmap, rmap, vmap;
+    if (!encode_bf16_2d(&qmap, q, (uint64_t)H * p.dq, (uint64_t)B * T) ||
+        !encode_bf16_2d(&kmap, k_up, (uint64_t)H * dn, (uint64_t)nr) ||
+        !encode_bf16_2d(&rmap, kv_cache, (uint64_t)(d + r), (uint64_t)nr) ||
+        !encode_bf16_2d(&vmap, v_up, (uint64_t)H * vd, (uint64_t)nr))
+        return DSA_ERR_CUDA;
+    return from_cuda(launch_mha(p, qmap, kmap, rmap, vmap, idx, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_device_error(void *stream, uint32_t *code) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return from_cuda(cudaErrorUnknown);
-    const uint32_t words[5] = {take_error_indexer(), take_error_topk(), take_error_mla(),
-                               take_error_append(), take_error_hisparse()};
+    const uint32_t words[6] = {take_error_indexer(), take_error_topk(), take_error_mla(),
+                               take_error_append(), take_error_hisparse(), take_error_mha()};
     uint32_t first = 0;
     for (uint32_t v : words) {
         if (v == 0xFFFFFFFFu) return DSA_ERR_CUDA;

@@ -168,6 +168,26 @@ void mla_split_plan(int rows, int k, int num_sms, int d, int *splits, int *tiles
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
 cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);
 
+// ---- MLA in MHA mode -------------------------------------------------------------------
+struct MhaParams {
+    const int32_t *q_pos;      // [B*T]
+    const int32_t *seq_start;  // [B] first cache row of each sequence (contiguous layout)
+    uint32_t *bitmap;          // [B*T, words] selection bitmaps (workspace)
+    uint16_t *out;             // [B*T, H, vd] bf16
+    float *lse;                // [B*T, H] or nullptr
+    int B, T, H, d, r, dn, dq, vd, k, Lmax, words;
+    float scale_log2;
+};
+// out[n, N] = X[n, :d] . W[N, d]^T (xmap: X as [n, ld] with 64 x 128 boxes; wmap: W as [N, d])
+cudaError_t launch_upproj(const CUtensorMap &xmap, const CUtensorMap &wmap, uint16_t *out, int n,
+                          int N, int d, cudaStream_t stream);
+// qmap: q as [B*T, H*dq]; kmap: k_up as [rows, H*dn]; rmap: the latent cache as [rows, d+r];
+// vmap: v_up as [rows, H*vd]; all with 64 x 128 boxes, 128-byte swizzle
+cudaError_t launch_mha(const MhaParams &p, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                       const CUtensorMap &rmap, const CUtensorMap &vmap, const int32_t *idx,
+                       cudaStream_t stream);
+uint32_t take_error_mha();
+
 // ---- host-tier working set (HiSparse) ----------------------------------------------------
 constexpr int kMaxHiSlots = 16384;  // device slots per sequence
 constexpr int kMaxHiK = 8192;       // index-row length
