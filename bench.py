@@ -428,6 +428,75 @@ def measure_hisparse(lay, dev, hbm_peak, C=4096, reps=10):
             "timing": "CUDA events around single launches, median of %d" % reps}
 
 
+def measure_mha_vs_mqa(dev, contexts=(2048, 4096, 8192), T=1024, H=64, reps=5):
+    """MLA's two modes on short-context chunked prefill: T query rows at the end of one
+    sequence, each with k = 2048 selected tokens (all of them when it sees fewer), the
+    GLM-5 shapes (latent 512 + rope 64; MHA mode: nope 192 + rope 64 per head, values of
+    128).  MHA mode: up-projection of the context's keys and values, then the masked
+    attention; MQA mode: the sparse MLA over the latent rows."""
+    import torch
+    from sparse_attention_29_b300 import capi, inputs
+    d, r, dn, vd, k = 512, 64, 192, 128, 2048
+    g = torch.Generator(device=dev).manual_seed(7)
+    w_uk = (torch.randn(H * dn, d, device=dev, generator=g) / 16).to(torch.bfloat16)
+    w_uv = (torch.randn(H * vd, d, device=dev, generator=g) / 16).to(torch.bfloat16)
+    out = {}
+    for L in contexts:
+        case = inputs.make_case(f"mha-{L}", seed=L, lengths=[L], T=T, H=H, k=k, device=dev)
+        n = L
+        idx = torch.full((T, k), -1, dtype=torch.int32, device=dev)
+        for t in range(T):
+            nv = int(case.q_pos[t]) + 1
+            m = min(nv, k)
+            idx[t, :m] = torch.sort(torch.randperm(nv, device=dev, generator=g)[:m]).values.to(torch.int32)
+        kv = case.kv[0]
+        q_mha = torch.randn(T, H, dn + r, device=dev, generator=g).to(torch.bfloat16)
+        k_up = torch.empty((n, H * dn), dtype=torch.bfloat16, device=dev)
+        v_up = torch.empty((n, H * vd), dtype=torch.bfloat16, device=dev)
+        o_mha = torch.empty((T, H, vd), dtype=torch.bfloat16, device=dev)
+        o_mqa = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        ws = capi.dsa_mha_workspace_bytes(1, T, L)
+        wbuf = torch.empty(ws, dtype=torch.uint8, device=dev)
+        wsm = capi.dsa_workspace_bytes(capi.DSA_OP_SPARSE_MLA, 1, T, H, d, k, 1)
+        wbm = torch.empty(max(wsm, 16), dtype=torch.uint8, device=dev)
+        layout = capi.make_layout(n, seq_start=case.seq_start)
+
+        def up():
+            capi.dsa_mla_up_project(kv, n, d + r, d, w_uk, H * dn, k_up)
+            capi.dsa_mla_up_project(kv, n, d + r, d, w_uv, H * vd, v_up)
+
+        def attn():
+            capi.dsa_sparse_mha_prefill(q_mha, k_up, v_up, kv, layout, idx, case.q_pos, 1, T, H, d,
+                                        r, dn, vd, k, L, case.softmax_scale, o_mha, lse, wbuf, ws)
+
+        def mqa():
+            capi.dsa_sparse_mla_prefill(case.q[0], kv, layout, idx, 1, T, H, d, r, k,
+                                        case.softmax_scale, o_mqa, lse, wbm, wsm)
+
+        def ms(fn):
+            fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        t_up, t_attn, t_mqa = ms(up), ms(attn), ms(mqa)
+        nsel = float(case.q_pos.long().add(1).clamp(max=k).sum().item())
+        out[str(L)] = {"mha_ms": t_up + t_attn, "mha_up_project_ms": t_up, "mha_attention_ms": t_attn,
+                       "mqa_sparse_mla_ms": t_mqa,
+                       "flops_per_pair": {"mha": 2 * H * (dn + r + vd), "mqa": 2 * H * (2 * d + r)},
+                       "selected_pairs": nsel}
+        del case, k_up, v_up
+    torch.cuda.empty_cache()
+    return {"rows": T, "heads": H, "shapes": "latent 512 + rope 64; MHA nope 192 + rope 64, values 128",
+            "by_context": out}
+
+
 def make_workload(name, device, seed_offset=0, rows=0):
     from sparse_attention_29_b300 import inputs
     if rows and inputs.PRESETS[name]["T"] > 1:
@@ -880,6 +949,10 @@ def main():
             except Exception as exc:
                 others[name] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
         line["other_workloads"] = others
+        try:  # MLA's two modes on short-context chunked prefill
+            line["mha_vs_mqa"] = measure_mha_vs_mqa(dev)
+        except Exception as exc:
+            line["mha_vs_mqa"] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
         try:  # the host-tier working set on the decode batch
             line["hisparse"] = measure_hisparse(layers[0], dev, hbm_peak)
         except Exception as exc:
