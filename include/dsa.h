@@ -240,8 +240,8 @@ dsa_status_t dsa_sparse_mla_shared(const uint16_t *const *q_layers,
  * 16-byte aligned.  n == 0 does nothing (the arrays may then be NULL).  A token whose
  * row does not resolve (sequence out of range, page entry missing or negative, row past
  * num_rows) is skipped and sets the device error word.  Tokens that map to the same row
- * race.  The kernel lets no later kernel of the stream start before it has finished
- * (the indexer reads the key cache without waiting).
+ * race.  The kernels that read the caches afterwards (indexer, sparse MLA) wait for the
+ * append's completion (griddepcontrol.wait) before their first cache read.
  */
 dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const int32_t *seq,
                               const int32_t *pos, int n, int B, int Di, int D,

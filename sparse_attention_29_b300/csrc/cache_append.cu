@@ -24,8 +24,8 @@
 // rounding to odd", IEEE Trans. Computers 2008).
 //
 // The kernel waits for its predecessor before touching memory and does not let its own
-// successor start early: the indexer reads the key cache without waiting (it treats its
-// inputs as step inputs), so it must not start before the new keys are written.
+// successor start early; the indexer that follows reads the key cache only after its own
+// griddepcontrol.wait, which waits for this kernel's completion and memory flush.
 #include "internal.h"
 #include "ptx.cuh"
 

@@ -310,12 +310,11 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     griddep_launch_dependents();
-    // Everything this kernel reads is a step input; only the score stores can conflict
-    // with earlier kernels in the stream (a previous top-k reading the same scores), so
-    // the epilogue warps alone wait for them (griddepcontrol.wait) before their first
-    // store, and the tile list, the query loads and the key stream start at once.  A
-    // kernel that does not trigger its dependents early has completed before this one
-    // starts at all.
+    // The tile list, the barriers and the tensor memory are set up while the previous
+    // kernel of the stream finishes; the producer waits for it (griddepcontrol.wait)
+    // before its first load, because that kernel may have written the key cache (a cache
+    // append), and the epilogue waits before its first store (a previous top-k may still
+    // read the scores).
 
     // ---- tile list: tiles of each query group, prefix-summed -------------------------
     {
@@ -469,6 +468,10 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
             __syncwarp();
             mbar_arrive(&qfull[slot]);
         };
+        // the keys and their scales may have just been written by the previous kernel of
+        // the stream (a cache append): the producer reads them only after
+        // griddepcontrol.wait, which waits for that kernel's completion and memory flush
+        griddep_wait();
         // the range's first group goes out before anything else
         {
             TileCursor c0;
