@@ -264,6 +264,27 @@ def kernel_times(layers, stream, steps, fns):
     return out
 
 
+def kernels_in_graph(graph):
+    """Kernel nodes of a captured CUDA graph (the launches one replay makes), or None."""
+    try:
+        from cuda.bindings import runtime as rt
+        raw = rt.cudaGraph_t(init_value=graph.raw_cuda_graph())
+        err, _, n = rt.cudaGraphGetNodes(raw, 0)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        err, nodes, n = rt.cudaGraphGetNodes(raw, n)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        count = 0
+        for node in nodes[:n]:
+            err, t = rt.cudaGraphNodeGetType(node)
+            if err == rt.cudaError_t.cudaSuccess and t == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                count += 1
+        return count
+    except Exception:
+        return None
+
+
 def step_of(case):
     return (lambda lay: lay.run_shared()) if case.layers > 1 else (lambda lay: lay.run())
 
@@ -710,9 +731,10 @@ def main():
         else:
             lay.run()
 
-    # indexer, top-k and sparse MLA; split rows merge inside the MLA kernel's clusters, and
-    # a separate merge kernel runs only when a row needs more splits than a cluster holds
-    # (fewer than SMs / 8 rows)
+    # launches per step: counted below from the kernel nodes of a captured step; before
+    # that (and if capture is unavailable) the calls' nominal count: the indexer, the top-k
+    # (inside the sparse MLA kernel in decode when the row fits), the sparse MLA, and a
+    # merge kernel when a row needs more splits than a cluster holds
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     launches_per_step = 3 + (1 if layers[0].ws_bytes and case.rows * 8 < sms else 0)
     for i in range(args.warmup):
@@ -749,10 +771,14 @@ def main():
     # are the previous steps' outputs), graph-replayed between events (kernel_times) ------
     if args.profile:  # no further launches after the timed steps
         k_idx = k_topk = k_mla = float("nan")
+        k_fused = None
     else:
         mla_call = (lambda lay: lay.mla_shared()) if shared else (lambda lay: lay.mla())
         k_idx, k_topk, k_mla = kernel_times(
             layers, stream, args.steps, [lambda lay: lay.indexer(), lambda lay: lay.topk(), mla_call])
+        k_fused = None
+        if case.T == 1 and not shared:  # top-k and sparse MLA in one call, as the step runs them
+            (k_fused,) = kernel_times(layers, stream, args.steps, [lambda lay: lay.topk_mla()])
 
     # ---- the same K steps replayed from a CUDA graph of the C-ABI calls ----------------
     graph_ms = None
@@ -786,6 +812,9 @@ def main():
         torch.cuda.synchronize()
         graph_ms = g0.elapsed_time(g1) / args.steps
         layers[0].check_device_error()
+        counted = kernels_in_graph(graphs[0])
+        if counted:
+            launches_per_step = counted
     except Exception as exc:  # graphs are an extra measurement; the step time stands
         graph_ms = f"unavailable: {type(exc).__name__}: {exc}"[:200]
         graphs = None
@@ -924,7 +953,8 @@ def main():
            if case.T > 1 else {}),
         "hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
         "step_bytes": step_bytes,
-        "kernel_ms": {"indexer": k_idx, "topk": k_topk, "sparse_mla": k_mla},
+        "kernel_ms": {"indexer": k_idx, "topk": k_topk, "sparse_mla": k_mla,
+                      **({"topk_and_sparse_mla_one_call": k_fused} if k_fused else {})},
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
         "graph_replay": (graph_ms if isinstance(graph_ms, str) else

@@ -159,6 +159,22 @@ dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
                                    uint16_t *out, float *lse, void *workspace,
                                    size_t workspace_bytes, void *stream);
 
+/*
+ * Top-K and sparse MLA decode in one call (§Lightning Indexer, §Sparse MLA): exactly
+ * dsa_topk(scores, q_pos, B, Lmax, k, idx) followed by dsa_sparse_mla_decode(..., idx, ...)
+ * -- same index set (written to idx), same outputs.  When a row's splits of the sparse
+ * MLA form one thread-block cluster (or are one CTA) and its scores fit their shared
+ * memory (about 26K scores per CTA at d = 512), one kernel does both: the cluster selects
+ * the row's index set, then attends over it; otherwise the top-k runs as its own launch
+ * first.  Arguments as the two calls; workspace as dsa_sparse_mla_decode.
+ */
+dsa_status_t dsa_topk_sparse_mla_decode(const float *scores, const int32_t *q_pos, int Lmax,
+                                        const uint16_t *q, const uint16_t *kv_cache,
+                                        const dsa_cache_layout_t *layout, int32_t *idx, int B,
+                                        int H, int d, int r, int k, float scale, uint16_t *out,
+                                        float *lse, void *workspace, size_t workspace_bytes,
+                                        void *stream);
+
 /* Size of the fixed device scratch behind dsa_sparse_mla_decode_noalloc (20 MiB). */
 #define DSA_NOALLOC_SCRATCH_BYTES ((size_t)20 << 20)
 

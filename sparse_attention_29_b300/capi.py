@@ -28,7 +28,7 @@ EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
            "dsa_sparse_mla_shared", "dsa_cache_append", "dsa_workspace_bytes",
            "dsa_device_error", "dsa_indexer_topk", "dsa_indexer_topk_workspace_bytes",
            "dsa_hisparse_init", "dsa_hisparse_fetch", "dsa_mla_up_project",
-           "dsa_mha_workspace_bytes", "dsa_sparse_mha_prefill")
+           "dsa_mha_workspace_bytes", "dsa_sparse_mha_prefill", "dsa_topk_sparse_mla_decode")
 
 
 class DsaError(RuntimeError):
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_hisparse_fetch.argtypes = [P, I, I, ctypes.c_uint32, P, P, I, P, I, P, P, I, P, P, P]
     lib.dsa_sparse_mla_decode.restype = I
     lib.dsa_sparse_mla_decode.argtypes = [P, P, LP, P, I, I, I, I, I, F, P, P, P, S, P]
+    lib.dsa_topk_sparse_mla_decode.restype = I
+    lib.dsa_topk_sparse_mla_decode.argtypes = [P, P, I, P, P, LP, P, I, I, I, I, I, F, P, P, P, S, P]
     lib.dsa_sparse_mla_decode_noalloc.restype = I
     lib.dsa_sparse_mla_decode_noalloc.argtypes = [P, P, LP, P, I, I, I, I, I, F, P, P, P]
     lib.dsa_sparse_mla_prefill.restype = I
@@ -221,6 +223,15 @@ def dsa_sparse_mla_decode(q, kv_cache, layout, idx, B, H, d, r, k, scale, out, l
                                       B, H, d, r, k, float(scale), _ptr(out), _ptr(lse),
                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("dsa_sparse_mla_decode", st)
+
+
+def dsa_topk_sparse_mla_decode(scores, q_pos, Lmax, q, kv_cache, layout, idx, B, H, d, r, k,
+                               scale, out, lse, workspace, workspace_bytes, stream=None):
+    st = load().dsa_topk_sparse_mla_decode(_ptr(scores), _ptr(q_pos), Lmax, _ptr(q),
+                                           _ptr(kv_cache), ctypes.byref(layout), _ptr(idx), B, H,
+                                           d, r, k, float(scale), _ptr(out), _ptr(lse),
+                                           _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check("dsa_topk_sparse_mla_decode", st)
 
 
 def dsa_sparse_mla_decode_noalloc(q, kv_cache, layout, idx, B, H, d, r, k, scale, out, lse,

@@ -75,11 +75,18 @@ int pow2_at_least(int x) {
     return p;
 }
 
+// fused top-k (decode): the row's scores, positions and score-row length; idx is written
+struct FusedTopk {
+    const float *scores;
+    const int32_t *q_pos;
+    int Lmax;
+};
+
 dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int n_layers,
                         const dsa_cache_layout_t *layout, const int32_t *idx, int B, int T,
                         int H, int d, int r, int k, float scale, uint16_t *const *out,
                         float *const *lse, void *workspace, size_t workspace_bytes,
-                        void *stream) {
+                        void *stream, const FusedTopk *ft = nullptr) {
     if (n_layers < 1 || n_layers > kMaxLayers) return DSA_ERR_INVALID_ARG;
     if (!q || !kv || !out || !idx || !layout) return DSA_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || r < 0 || k <= 0) return DSA_ERR_INVALID_ARG;
@@ -124,6 +131,30 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
     }
     // TMA descriptors: q as [rows*H, D] (64-row x 64-column boxes), kv as [num_rows, D]
     // (one-row boxes for gather4), bf16, 128-byte swizzle
+    if (ft) {
+        // the row's splits select its index set first when they form one cluster (or are
+        // one CTA) and the row's scores fit their tile buffers; otherwise a separate top-k
+        // launch comes first
+        const int slice = n_layers == 1 ? mla_topk_slice(ft->Lmax, p.splits, d) : 0;
+        if (slice > 0) {
+            p.topk = 1;
+            p.topk_slice = slice;
+            p.scores = ft->scores;
+            p.q_pos = ft->q_pos;
+            p.Lmax = ft->Lmax;
+            p.idx_out = const_cast<int32_t *>(idx);
+        } else {
+            TopkParams tp;
+            tp.scores = ft->scores;
+            tp.q_pos = ft->q_pos;
+            tp.idx = const_cast<int32_t *>(idx);
+            tp.rows = B * T;
+            tp.Lmax = ft->Lmax;
+            tp.k = k;
+            const cudaError_t e = launch_topk(tp, sms, static_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+    }
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_tiled();
     if (!encode) return DSA_ERR_CUDA;
     MlaMaps maps;
@@ -393,6 +424,22 @@ dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
                                    size_t workspace_bytes, void *stream) {
     return mla_common(&q, &kv_cache, 1, layout, idx, B, 1, H, d, r, k, scale, &out,
                       lse ? &lse : nullptr, workspace, workspace_bytes, stream);
+}
+
+dsa_status_t dsa_topk_sparse_mla_decode(const float *scores, const int32_t *q_pos, int Lmax,
+                                        const uint16_t *q, const uint16_t *kv_cache,
+                                        const dsa_cache_layout_t *layout, int32_t *idx, int B,
+                                        int H, int d, int r, int k, float scale, uint16_t *out,
+                                        float *lse, void *workspace, size_t workspace_bytes,
+                                        void *stream) {
+    if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
+    if (Lmax <= 0) return DSA_ERR_INVALID_ARG;
+    FusedTopk ft;
+    ft.scores = scores;
+    ft.q_pos = q_pos;
+    ft.Lmax = Lmax;
+    return mla_common(&q, &kv_cache, 1, layout, idx, B, 1, H, d, r, k, scale, &out,
+                      lse ? &lse : nullptr, workspace, workspace_bytes, stream, &ft);
 }
 
 dsa_status_t dsa_sparse_mla_decode_noalloc(const uint16_t *q, const uint16_t *kv_cache,

@@ -154,6 +154,15 @@ struct MlaParams {
     int tiles_per_split;
     int cluster;       // 1: the splits of a (row, layer) form a thread-block cluster and
                        // merge their partial results through the workspace
+    // top-k in the same launch (decode): the splits of each row first select the row's
+    // index set from `scores` (the row's cluster runs the cluster top-k, slices of
+    // topk_slice scores) and write it to idx_out (= idx), then attend over it
+    int topk;
+    int topk_slice;
+    const float *scores;
+    const int32_t *q_pos;
+    int Lmax;
+    int32_t *idx_out;
 };
 
 // TMA descriptors of every layer: q viewed as [rows*H, d+r], kv as [num_rows, d+r] (bf16)
@@ -167,6 +176,10 @@ int mla_tile_keys();  // keys per sparse MLA tile (the split unit)
 void mla_split_plan(int rows, int k, int num_sms, int d, int *splits, int *tiles_per_split);
 size_t mla_partial_bytes(int rows_times_layers, int splits, int d);
 cudaError_t launch_sparse_mla(const MlaParams &p, const MlaMaps &maps, cudaStream_t stream);
+// The slice size (scores per CTA) at which a row's top-k can run inside the sparse MLA
+// kernel with `splits` CTAs per row for latent width d, or 0 when it cannot (no cluster
+// for the splits, or the slice does not fit the kernel's tile buffers).
+int mla_topk_slice(int Lmax, int splits, int d);
 
 // ---- MLA in MHA mode -------------------------------------------------------------------
 struct MhaParams {

@@ -75,6 +75,11 @@ __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// End an mbarrier's life before its shared memory is used for anything else.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -214,6 +219,14 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
 __device__ __forceinline__ int ldg_early(const int *ptr) {
     int v;
     asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
+// The same through L2 only (coherent with other SMs' stores made visible before a
+// barrier of the same kernel).
+__device__ __forceinline__ int ldcg_early(const int *ptr) {
+    int v;
+    asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
     return v;
 }
 

@@ -55,6 +55,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "topk_core.cuh"
 
 namespace dsa {
 namespace {
@@ -246,12 +247,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < nch; ++c)
             tma_load_2d(qs + c * kQChunkBytes, qmap, q_full, c * 64, row * p.H);
     }
-    griddep_wait();  // the index set comes from the previous kernel
-    // the resolving gather lanes fetch tile 0's token indices first
+    griddep_wait();  // the index set (or the scores) come from the previous kernel
+    if (p.topk) {
+        // this row's top-k first, by the row's splits (the cluster), in the tile buffers
+        // (free until the gathers start); the index set then comes back from L2
+        TopkParams tp;
+        tp.scores = p.scores;
+        tp.q_pos = p.q_pos;
+        tp.idx = p.idx_out;
+        tp.rows = p.B * p.T;
+        tp.Lmax = p.Lmax;
+        tp.k = p.k;
+        tk::topk_row(tp, row, p.splits, p.cluster ? cluster_rank() : 0u, p.topk_slice, tiles);
+        __threadfence();
+        if (p.cluster) cluster_sync();
+        else __syncthreads();
+    }
+    // the resolving gather lanes fetch tile 0's token indices first (through L2: in one
+    // launch with the top-k they were written by this cluster a moment ago)
     int s_pre = -1;
     if (resolver && ntiles > 0) {
         const int j = t_begin * kTileKeys + my_row;
-        if (j < p.k) s_pre = __ldg(idx_row + j);
+        if (j < p.k) s_pre = ldcg_early(idx_row + j);
     }
     const uint32_t tS = tmem;          // [2 buffers][2 issuer parts] x 64 columns
     const uint32_t tO = tmem + 256;    // nmb x 64 columns
@@ -355,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a valid token index that does not resolve is an error.
         auto idx_at = [&](int li) -> int {  // token index of this lane's row in tile li
             const int j = (t_begin + li) * kTileKeys + my_row;
-            return (resolver && li < ntiles && j < p.k) ? ldg_early(idx_row + j) : -1;
+            return (resolver && li < ntiles && j < p.k) ? ldcg_early(idx_row + j) : -1;
         };
         auto page_of = [&](int s) -> int {  // block-table entry of token s, or -1
             if (!paged || s < 0) return -1;
@@ -427,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto key_valid = [&](int li, int key) -> bool {
             const int j = (t_begin + li) * kTileKeys + key;
             if (li >= ntiles || j >= p.k) return false;
-            const int s = __ldg(idx_row + j);
+            const int s = __ldcg(idx_row + j);
             return s >= 0 && resolve_row(p.layout, b, s) >= 0;
         };
         if (warp == 0) {
@@ -849,6 +866,13 @@ void mla_split_plan(int units, int k, int num_sms, int d, int *splits_out, int *
 }
 
 bool mla_cluster_merge(int splits) { return splits > 1 && splits <= kMaxClusterSplits; }
+
+int mla_topk_slice(int Lmax, int splits, int d) {
+    if (splits < 1 || splits > kMaxClusterSplits || Lmax <= 0) return 0;
+    const int slice = (((Lmax + splits - 1) / splits) + 31) & ~31;
+    const uint32_t tile_bytes = 2u * (uint32_t)(d / 64 + 1) * kChunkBytes;
+    return tk::topk_layout(slice).total <= tile_bytes ? slice : 0;
+}
 
 size_t mla_partial_bytes(int units, int splits, int d) {
     if (splits <= 1) return 0;

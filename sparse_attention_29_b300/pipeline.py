@@ -2,6 +2,7 @@
 
     layer = DsaLayer(case_on_gpu)
     layer.run()          # indexer -> top-k -> sparse MLA, all in libdsa's kernels
+                         # (decode: top-k and sparse MLA in one call)
     layer.run_shared()   # IndexShare: indexer and top-k once, MLA for every layer
 
 Only allocation and argument marshalling happen here.
@@ -76,6 +77,14 @@ class DsaLayer:
                                           self.lse[layer], self.workspace, self.ws_bytes,
                                           self.stream)
 
+    def topk_mla(self, layer=0):
+        """Top-k and sparse MLA decode in one call (one kernel where the row fits)."""
+        c = self.case
+        libdsa.dsa_topk_sparse_mla_decode(self.scores, c.q_pos, c.Lmax, c.q[layer], c.kv[layer],
+                                          self.layout, self.idx, c.B, c.H, c.d, c.r, c.k,
+                                          c.softmax_scale, self.out[layer], self.lse[layer],
+                                          self.workspace, self.ws_bytes, self.stream)
+
     def mla_shared(self, idx=None):
         c = self.case
         idx = self.idx if idx is None else idx
@@ -86,8 +95,11 @@ class DsaLayer:
     # -- whole steps --------------------------------------------------------------------
     def run(self, layer=0):
         self.indexer()
-        self.topk()
-        self.mla(layer)
+        if self.case.T == 1:
+            self.topk_mla(layer)
+        else:
+            self.topk()
+            self.mla(layer)
 
     def run_shared(self):
         self.indexer()

@@ -217,3 +217,26 @@ def test_shared_equals_separate_layer_calls():
     torch.cuda.synchronize()
     for g in range(3):
         assert torch.equal(shared[g], lay.out[g])
+
+
+@pytest.mark.parametrize("lengths", [
+    [3000] * 32,            # 4 splits per row: the row's cluster selects, then attends
+    [5000, 3000, 2100],     # more splits than a cluster holds: a separate top-k launch first
+    [2600] * 160,           # one CTA per row selects and attends
+    [1500, 2049, 2048] * 12,  # dense rows and the dense edge
+])
+def test_topk_and_mla_in_one_call_equal_the_two_calls(lengths):
+    case = inputs.make_case(kind="planted", seed=len(lengths), lengths=lengths, T=1)
+    lay = gpu_layer(case)
+    lay.indexer()
+    lay.topk()
+    lay.mla()
+    torch.cuda.synchronize()
+    idx_sep, out_sep, lse_sep = lay.idx.clone(), lay.out[0].clone(), lay.lse[0].clone()
+    lay.idx.fill_(-7)
+    lay.out[0].zero_()
+    lay.topk_mla()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    assert torch.equal(lay.idx, idx_sep)
+    assert torch.equal(lay.out[0], out_sep) and torch.equal(lay.lse[0], lse_sep)
