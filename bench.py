@@ -678,6 +678,9 @@ def main():
                          "a smaller case of the same kernel, e.g. for profiler captures)")
     ap.add_argument("--fused", action="store_true",
                     help="prefill workloads: the step uses the fused indexer + top-k")
+    ap.add_argument("--two-call", action="store_true",
+                    help="decode: the step runs top-k and sparse MLA as two calls (the "
+                         "API's other form) instead of the one-call decode")
     ap.add_argument("--append-only", action="store_true",
                     help="only the cache-append measurement (one JSON object; for profiler "
                          "captures of that kernel)")
@@ -728,6 +731,10 @@ def main():
             lay.run_shared()
         elif args.fused and case.T > 1:
             lay.run_fused()
+        elif args.two_call:
+            lay.indexer()
+            lay.topk()
+            lay.mla()
         else:
             lay.run()
 
@@ -795,9 +802,10 @@ def main():
                 step(lay)  # warm the per-kernel attribute set-up outside capture
             torch.cuda.synchronize()
             for lay in layers:
-                g = torch.cuda.CUDAGraph()
+                g = torch.cuda.CUDAGraph(keep_graph=True)  # kept for the node count below
                 with torch.cuda.graph(g, stream=cap):
                     step(lay)
+                g.instantiate()
                 graphs.append(g)
         for lay in layers:
             lay.stream = None
@@ -946,7 +954,11 @@ def main():
                    "batch": case.B, "rows": case.rows, "context": case.lengths[0] if len(set(case.lengths)) == 1 else "ragged",
                    "k": case.k, "layers": case.layers, "page_size": case.page_size,
                    "l2": f"inputs larger than L2, {args.sets} rotating input sets",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "step_calls": ("indexer, top-k and MLA over shared layers" if shared else
+                                  "fused indexer + top-k, then MLA" if args.fused and case.T > 1
+                                  else "indexer, top-k, MLA" if args.two_call or case.T > 1
+                                  else "indexer, then top-k + MLA in one call")},
         "hbm_tbs": step_bytes / (ms_per_step * 1e-3) / 1e12,
         **({"hbm_note": "per-row algorithmic bytes: the rows of one sequence share its keys "
                         "and many selected rows, so much of this is served from L2"}

@@ -641,21 +641,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (p.cluster) {
         // ===== merge the cluster's splits: CTA `split` finishes dims [d_lo, d_hi) =====
-        // The unnormalised O goes to this split's slot of the workspace as [64 heads][d]
-        // bf16 (all 16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31, the latent dims,
-        // columns 16 (w / 4) .. +15, the heads; consecutive threads store consecutive
-        // dims); after the cluster barrier each CTA reads its slice of every split back
-        // from L2.  The exchange is L2-bandwidth-bound, so it moves bf16: one more
-        // rounding (relative 2^-9) ahead of a four-term weighted sum whose result is
-        // rounded to bf16 anyway.  The maxima and sums (rn, lsum) stay in shared memory.
-        const size_t stride = (size_t)(kHeads * p.d + 2 * kHeads);
+        // Every CTA writes its unnormalised O to its slot of the workspace as bf16 in
+        // [head][dim] order (all 16 warps: warp w reads TMEM lanes 32 (w % 4) .. +31, the
+        // latent dims, columns 16 (w / 4) .. +15, the heads; consecutive threads store
+        // consecutive dims), then its running maxima and sums.  After one cluster barrier
+        // each CTA reads its slice of every split's slot back from L2 (16-byte loads of 8
+        // dims, issued before the weights are known), weighs and sums them in split order
+        // and writes the output.  No CTA reads another's shared memory, so none waits for
+        // the others once its slice is written.  The exchange moves bf16: one more
+        // rounding (relative 2^-9) ahead of a weighted sum of at most eight terms whose
+        // result is rounded to bf16 anyway.
+        const size_t stride = (size_t)(kHeads * p.d + 2 * kHeads);  // floats per split slot
         const int unit_out = row * p.layers + layer;
         float *part_base = p.partial + (int64_t)unit_out * p.splits * stride;
         __syncthreads();  // the softmax warps have seen O complete; rn, lsum final
         tc_fence_after();
         {
             const bool valid_o = *have_o_sm != 0;
-            uint16_t *part = reinterpret_cast<uint16_t *>(part_base + (size_t)split * stride);
+            float *slot = part_base + (size_t)split * stride;
+            uint16_t *po = reinterpret_cast<uint16_t *>(slot);
             const int q = warp & 3, cg = warp >> 2;
             // every M-block's 16 columns are loaded before one wait
             uint32_t v[4][16];
@@ -669,23 +673,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (mb < nmb && dim < p.d) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        part[(int64_t)(16 * cg + e) * p.d + dim] =
+                        po[(int64_t)(16 * cg + e) * p.d + dim] =
                             valid_o ? __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[mb][e]))) : (uint16_t)0;
                 }
+            }
+            if (tid < kHeads) {
+                slot[kHeads * p.d + tid] = valid_o ? rn[tid] : -INFINITY;
+                slot[kHeads * p.d + kHeads + tid] = valid_o ? lsum[tid] : 0.f;
             }
         }
         tc_fence_before();
         __threadfence();
-        cluster_sync();  // every split's O (global), maxima and sums (shared) are in place
-        float *wts = (float *)(smem + L.wts);
+        cluster_sync();  // every split's O, maxima and sums are in the workspace
+        float *wts = (float *)(smem + L.wts);  // [split][head] weights
+        const int ds = ((p.d + p.splits - 1) / p.splits + 7) & ~7;
+        const int d_lo = min(p.d, split * ds), d_hi = min(p.d, d_lo + ds);
+        const int ng = (d_hi - d_lo) >> 3;  // groups of 8 dims
+        const int n_items = ng * kHeads;    // (head, 8 dims); consecutive threads: dims
+        const uint16_t *pbase = reinterpret_cast<const uint16_t *>(part_base);
+        uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
+        auto load_item = [&](int it, uint4 (&v)[kMaxClusterSplits]) {
+            const int h = it / max(ng, 1), dim = d_lo + 8 * (it - h * ng);
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s)
+                v[s] = (s < p.splits && it < n_items)
+                           ? __ldcg(reinterpret_cast<const uint4 *>(pbase + (size_t)s * stride * 2 +
+                                                                    (int64_t)h * p.d + dim))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        };
+        auto finish_item = [&](int it, const uint4 (&v)[kMaxClusterSplits]) {
+            if (it >= n_items) return;
+            const int h = it / ng, dim = d_lo + 8 * (it - h * ng);
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                if (s >= p.splits) break;
+                const float w = wts[s * kHeads + h];
+                const uint32_t u[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] = fmaf(w, __uint_as_float(u[e] << 16), acc[2 * e]);
+                    acc[2 * e + 1] = fmaf(w, __uint_as_float(u[e] & 0xFFFF0000u), acc[2 * e + 1]);
+                }
+            }
+            if (h < p.H) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+                    pk[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                *reinterpret_cast<uint4 *>(out + (int64_t)h * p.d + dim) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        };
+        // this thread's first two items: their loads go out before the weights are known
+        uint4 va[kMaxClusterSplits], vb[kMaxClusterSplits];
+        load_item(tid, va);
+        load_item(tid + kThreads, vb);
         if (tid < kHeads) {
             // every split's maximum and sum for head h, all loads in flight at once
             const int h = tid;
             float rs[kMaxClusterSplits], ls[kMaxClusterSplits];
 #pragma unroll
             for (int s = 0; s < kMaxClusterSplits; ++s) {
-                rs[s] = s < p.splits ? __uint_as_float(dsmem_ld(&rn[h], (uint32_t)s)) : -INFINITY;
-                ls[s] = s < p.splits ? __uint_as_float(dsmem_ld(&lsum[h], (uint32_t)s)) : 0.f;
+                rs[s] = s < p.splits ? __ldcg(part_base + s * stride + kHeads * p.d + h) : -INFINITY;
+                ls[s] = s < p.splits ? __ldcg(part_base + s * stride + kHeads * p.d + kHeads + h) : 0.f;
             }
             float R = -INFINITY;  // raw logit units, like every split's maximum
 #pragma unroll
@@ -704,43 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     Lsum > 0.f ? (R * p.scale_log2 + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         }
         __syncthreads();
-        const int ds = ((p.d + p.splits - 1) / p.splits + 3) & ~3;
-        const int d_lo = min(p.d, split * ds), d_hi = min(p.d, d_lo + ds);
-        const int ng = (d_hi - d_lo) >> 2;  // groups of 4 dims
-        uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
-#pragma unroll 2
-        for (int it = tid; it < ng * kHeads; it += kThreads) {
-            const int h = it / ng, dim = d_lo + 4 * (it - h * ng);  // consecutive threads: dims
-            const uint16_t *src = reinterpret_cast<const uint16_t *>(part_base) + (int64_t)h * p.d + dim;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s0 = 0; s0 < kMaxClusterSplits; s0 += 4) {
-                if (s0 >= p.splits) break;
-                uint2 v[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v[e] = s0 + e < p.splits
-                               ? __ldcg(reinterpret_cast<const uint2 *>(src + (size_t)(s0 + e) * stride * 2))
-                               : make_uint2(0u, 0u);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float w = wts[(s0 + e) * kHeads + h];
-                    acc.x = fmaf(w, __uint_as_float(v[e].x << 16), acc.x);
-                    acc.y = fmaf(w, __uint_as_float(v[e].x & 0xFFFF0000u), acc.y);
-                    acc.z = fmaf(w, __uint_as_float(v[e].y << 16), acc.z);
-                    acc.w = fmaf(w, __uint_as_float(v[e].y & 0xFFFF0000u), acc.w);
-                }
-            }
-            if (h < p.H) {
-                const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
-                const __nv_bfloat162 c = __floats2bfloat162_rn(acc.z, acc.w);
-                uint2 pk;
-                pk.x = *reinterpret_cast<const uint32_t *>(&a);
-                pk.y = *reinterpret_cast<const uint32_t *>(&c);
-                *reinterpret_cast<uint2 *>(out + (int64_t)h * p.d + dim) = pk;
-            }
+        finish_item(tid, va);
+        finish_item(tid + kThreads, vb);
+        for (int it = tid + 2 * kThreads; it < n_items; it += 2 * kThreads) {
+            load_item(it, va);
+            load_item(it + kThreads, vb);
+            finish_item(it, va);
+            finish_item(it + kThreads, vb);
         }
-        cluster_sync();  // no CTA leaves while a peer may still read its maxima and sums
     }
 
     tc_fence_before();
