@@ -479,6 +479,10 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
             load_group(c0.g, 0);
         }
         int it = 0, gcount = 1, issued = 0;
+        // a sequence's keys are read by one query group only when its rows form one group
+        // (decode): then they are a stream read once, and L2 keeps them last
+        const bool read_once = p.groups_per_seq == 1;
+        const uint64_t kpol = policy_evict_first();
         int pstage = 0, pslot = 0;
         uint32_t pphase = 0;
         bool ok = true;
@@ -568,7 +572,14 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                     if (ok) {
                         uint8_t *dst = kstage + stage * kTileBytes;
                         mbar_arrive_expect_tx(&kfull[stage], (uint32_t)(nbox * kBoxRows * DI));
-                        if (nbox == 2 && y1 == y0 + kBoxRows) {
+                        if (read_once) {  // keys no other query group reads: evict first
+                            if (nbox == 2 && y1 == y0 + kBoxRows) {
+                                tma_load_2d_hint(dst, &kmap128, &kfull[stage], 0, y0, kpol);  // one 128-row box
+                            } else {
+                                if (nbox > 0) tma_load_2d_hint(dst, &kmap, &kfull[stage], 0, y0, kpol);
+                                if (nbox > 1) tma_load_2d_hint(dst + kBoxRows * DI, &kmap, &kfull[stage], 0, y1, kpol);
+                            }
+                        } else if (nbox == 2 && y1 == y0 + kBoxRows) {
                             tma_load_2d(dst, &kmap128, &kfull[stage], 0, y0);  // one 128-row box
                         } else {
                             if (nbox > 0) tma_load_2d(dst, &kmap, &kfull[stage], 0, y0);

@@ -188,6 +188,33 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
+// An L2 policy for data read once: its lines are the first to be evicted, so that a
+// stream larger than L2 does not push out what the next kernels of a step reuse (their
+// code, the scores, the index sets, the per-step inputs).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_2d with an L2 cache policy (policy_evict_first()).
+__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map,
+                                                 uint64_t *bar, int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// cp_async_16 with an L2 cache policy (policy_evict_first()).
+__device__ __forceinline__ void cp_async_16_hint(void *smem_dst, const void *gmem_src,
+                                                 uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared; src_bytes < 16 zero-fills the rest
 // (src_bytes == 0 reads nothing).
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src,

@@ -397,6 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // thread gt copies 16-byte granule (gt & 7) of chunk c for rows (gt >> 3) and
         // (gt >> 3) + 32, chunk by chunk, each chunk as soon as its space is free
         const int gi = gt & 7, ra = gt >> 3, rb = ra + 32;
+        // decode (one query row per sequence): a selected row is read by this row only, so
+        // the gathered rows are a stream read once, and L2 keeps them last; the query rows
+        // of a prefill chunk select many of the same rows, which stay in L2 as usual
+        const bool read_once = p.T == 1;
+        const uint64_t rpol = policy_evict_first();
         for (int li = 0; li < ntiles; ++li) {
             const int bi = li & 1;
             uint8_t *buf = tiles + bi * buf_bytes;
@@ -417,8 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool in = c < nv || gi * 8 < p.r;
                     const int off = c * 128 + gi * 16;
                     uint8_t *dst = buf + c * kChunkBytes + ((gi ^ (ra & 7)) << 4);
-                    cp_async_16(dst + ra * 128, (in && pa) ? pa + off : kv_bytes, (in && pa) ? 16u : 0u);
-                    cp_async_16(dst + rb * 128, (in && pb) ? pb + off : kv_bytes, (in && pb) ? 16u : 0u);
+                    const void *sa = (in && pa) ? pa + off : kv_bytes, *sb = (in && pb) ? pb + off : kv_bytes;
+                    const uint32_t na = (in && pa) ? 16u : 0u, nb = (in && pb) ? 16u : 0u;
+                    if (read_once) {
+                        cp_async_16_hint(dst + ra * 128, sa, na, rpol);
+                        cp_async_16_hint(dst + rb * 128, sb, nb, rpol);
+                    } else {
+                        cp_async_16(dst + ra * 128, sa, na);
+                        cp_async_16(dst + rb * 128, sb, nb);
+                    }
                 }
                 cp_async_arrive(&full[bi * 9 + c]);
             }
