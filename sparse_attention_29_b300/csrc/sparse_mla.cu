@@ -402,6 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of a prefill chunk select many of the same rows, which stay in L2 as usual
         const bool read_once = p.T == 1;
         const uint64_t rpol = policy_evict_first();
+        // chunks go in the order their space is freed: the two O issuers' M-blocks
+        // interleave (0, a, 1, a + 1, ...), the rope chunk (it held P) comes last; 4 bits
+        // per position
+        uint64_t corder = 0;
+        {
+            const int nmb_a = (nmb + 1) / 2;
+            int pos = 0;
+            for (int q = 0; q < nmb; ++q) {
+                const int mb = (q & 1) ? nmb_a + (q >> 1) : (q >> 1);
+                for (int w = 0; w < 2 && 2 * mb + w < nv; ++w) corder |= (uint64_t)(2 * mb + w) << (4 * pos++);
+            }
+            corder |= (uint64_t)rope << (4 * pos);
+        }
         for (int li = 0; li < ntiles; ++li) {
             const int bi = li & 1;
             uint8_t *buf = tiles + bi * buf_bytes;
@@ -412,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pg_nx = page_of(s_nx);  // both loads complete while this tile is copied
             const int s_nn = idx_at(li + 2);
             bool fail = false;
-            for (int c = 0; c < nch; ++c) {
+            for (int cpos = 0; cpos < nch; ++cpos) {
+                const int c = (int)((corder >> (4 * cpos)) & 15u);
                 if (li >= 2 && !fail) {
                     const uint32_t par = ((li - 2) >> 1) & 1;
                     if (c == rope) fail = !mbar_wait(&tfree_p[bi], par, KID_MLA, abort_flag);
