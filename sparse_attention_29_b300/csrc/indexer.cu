@@ -58,7 +58,7 @@ constexpr int kBoxRows = 64;
 
 struct Smem {
     // offsets (bytes) from the 1024-aligned dynamic shared memory base
-    uint32_t kstage, qbuf, qbuf_bytes, ksring, wbuf, gpos, prefix, sel, bars, total;
+    uint32_t kstage, qbuf, qbuf_bytes, ksring, wbuf, gpos, prefix, gmax, sel, bars, total;
     int ring;
 };
 
@@ -92,6 +92,8 @@ __host__ __device__ inline Smem smem_layout(int Di, int N, int stages, int num_g
     off += 2 * 16 * 4;
     s.prefix = off;
     off += ((uint32_t)num_groups + 1 + 3) / 4 * 16;
+    s.gmax = off;  // each group's largest valid position (from the tile list)
+    off += ((uint32_t)num_groups + 3) / 4 * 16;
     s.sel = off;  // [rows][kCoarseBins] counts, [4][16] per-row counters, staging
     off += (uint32_t)sel_rows * kCoarseBins * 4 + (sel_rows ? 4 * 16 * 4 : 0);
     off = (off + 15) & ~15u;
@@ -184,15 +186,14 @@ struct GroupWalk {
 };
 
 // Largest valid position among the rows of query group g (-1 if none).
-__device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool report,
-                                            bool early = false) {
+__device__ __forceinline__ int group_maxpos(const IndexerParams &p, int g, bool report) {
     const int b = g / p.groups_per_seq;
     const int gi = g - b * p.groups_per_seq;
     const int r0 = b * p.T + gi * p.G;
     const int nr = min(p.G, p.T - gi * p.G);
     int maxpos = -1;
     for (int i = 0; i < nr; ++i) {
-        const int pos = early ? ldg_early(p.q_pos + r0 + i) : __ldg(p.q_pos + r0 + i);
+        const int pos = __ldg(p.q_pos + r0 + i);
         if (pos < 0 || pos >= p.Lmax) {
             if (report) record_error(KID_INDEXER, ERR_BAD_POSITION);
             continue;
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
     float *wbuf = (float *)(smem + L.wbuf);
     int *gpos = (int *)(smem + L.gpos);
     int *prefix = (int *)(smem + L.prefix);
+    int *gmax = (int *)(smem + L.gmax);
     uint64_t *bars = (uint64_t *)(smem + L.bars);
     uint64_t *kfull = bars;
     uint64_t *kempty = kfull + p.stages;
@@ -324,7 +326,9 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         const int lo = min(tid * per, ng), hi = min(lo + per, ng);
         int local = 0;
         for (int g = lo; g < hi; ++g) {
-            const int n = (group_maxpos(p, g, blockIdx.x == 0) + kTileKeys) / kTileKeys;
+            const int mp = group_maxpos(p, g, blockIdx.x == 0);
+            gmax[g] = mp;
+            const int n = (mp + kTileKeys) / kTileKeys;
             prefix[g] = n;  // counts first, offsets below
             local += n;
         }
@@ -449,22 +453,24 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                 }
                 fence_proxy_async();
             }
+            // the position first, then two weights per lane, all in flight before any use
+            const int pos = (lane < 16 && lane < nr) ? __ldg(p.q_pos + r0 + lane) : -1;
             float *wdst = wbuf + slot * p.N;
-            for (int n = lane; n < p.N; n += 32) {
-                const int qi = n / p.HP, h = n - qi * p.HP;
-                float v = 0.f;
-                if (qi < nr && h < p.Hi)
-                    v = __ldg(p.w + (int64_t)(r0 + qi) * p.Hi + h) * __ldg(p.q_scale + r0 + qi);
-                wdst[n] = v;
-            }
-            if (lane < 16) {
-                int pos = -1;
-                if (lane < nr) {
-                    pos = __ldg(p.q_pos + r0 + lane);
-                    if (pos < 0 || pos >= p.Lmax) pos = -1;
+            for (int n0 = lane; n0 < p.N; n0 += 64) {
+                float v[2], sc[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int n = n0 + 32 * u;
+                    const int qi = n / p.HP, h = n - qi * p.HP;
+                    const bool in = n < p.N && qi < nr && h < p.Hi;
+                    v[u] = in ? __ldg(p.w + (int64_t)(r0 + qi) * p.Hi + h) : 0.f;
+                    sc[u] = in ? __ldg(p.q_scale + r0 + qi) : 0.f;
                 }
-                gpos[slot * 16 + lane] = pos;
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    if (n0 + 32 * u < p.N) wdst[n0 + 32 * u] = v[u] * sc[u];
             }
+            if (lane < 16) gpos[slot * 16 + lane] = (pos < 0 || pos >= p.Lmax) ? -1 : pos;
             __syncwarp();
             mbar_arrive(&qfull[slot]);
         };
@@ -472,12 +478,6 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         // the stream (a cache append): the producer reads them only after
         // griddepcontrol.wait, which waits for that kernel's completion and memory flush
         griddep_wait();
-        // the range's first group goes out before anything else
-        {
-            TileCursor c0;
-            c0.init(prefix, p.num_groups, tb, te);
-            load_group(c0.g, 0);
-        }
         int it = 0, gcount = 1, issued = 0;
         // a sequence's keys are read by one query group only when its rows form one group
         // (decode): then they are a stream read once, and L2 keeps them last
@@ -489,8 +489,10 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
         // ---- lane l resolves tile it0 + l of a batch in two phases: the raw loads (group,
         // cache page or sequence start, query positions) go out a whole batch ahead, and
         // the box rows are derived from them after the current batch has been issued ----
+        // (fetch only moves loaded values into registers; finish() uses them, so nothing
+        // here waits for a load in flight)
         int f_g = 0, f_newg = 0, f_s0 = 0, f_maxpos = -1, f_pg0 = -1, f_pg1 = -1, f_on = 0;
-        int64_t f_st = 0;
+        int f_st = 0, f_lp = 0;
         auto fetch = [&](int it0) {
             const int nbf = min(kBatch, ntile - it0);
             f_on = lane < nbf;
@@ -504,12 +506,13 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                 if (p.layout.block_table) {
                     const int lp0 = f_s0 / p.layout.page_size, lp1 = (f_s0 + kBoxRows) / p.layout.page_size;
                     const int *bt = p.layout.block_table + (int64_t)b * p.layout.pages_per_seq;
-                    f_pg0 = lp0 < p.layout.pages_per_seq ? ldg_early(bt + lp0) : -1;
-                    f_pg1 = lp1 < p.layout.pages_per_seq ? ldg_early(bt + lp1) : -1;
+                    f_lp = (lp0 < p.layout.pages_per_seq ? 1 : 0) | (lp1 < p.layout.pages_per_seq ? 2 : 0);
+                    f_pg0 = ldg_early(bt + ((f_lp & 1) ? lp0 : 0));
+                    f_pg1 = ldg_early(bt + ((f_lp & 2) ? lp1 : 0));
                 } else {
                     f_st = ldg_early(p.layout.seq_start + b);
                 }
-                f_maxpos = group_maxpos(p, c.g, false, true);
+                f_maxpos = gmax[c.g];
             }
         };
         int l_g = 0, l_newg = 0, l_nbox = 0, l_y0 = 0, l_y1 = 0, l_r0 = -1, l_r1 = -1;
@@ -522,11 +525,12 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
             if (!f_on) return;
             int64_t yb[2];
             if (p.layout.block_table) {
-                yb[0] = f_pg0 < 0 ? -1 : (int64_t)f_pg0 * p.layout.page_size + f_s0 % p.layout.page_size;
-                yb[1] = f_pg1 < 0 ? -1 : (int64_t)f_pg1 * p.layout.page_size + (f_s0 + kBoxRows) % p.layout.page_size;
+                const int pg0 = (f_lp & 1) ? f_pg0 : -1, pg1 = (f_lp & 2) ? f_pg1 : -1;
+                yb[0] = pg0 < 0 ? -1 : (int64_t)pg0 * p.layout.page_size + f_s0 % p.layout.page_size;
+                yb[1] = pg1 < 0 ? -1 : (int64_t)pg1 * p.layout.page_size + (f_s0 + kBoxRows) % p.layout.page_size;
             } else {
-                yb[0] = f_st + f_s0;
-                yb[1] = f_st + f_s0 + kBoxRows;
+                yb[0] = (int64_t)f_st + f_s0;
+                yb[1] = (int64_t)f_st + f_s0 + kBoxRows;
             }
             int ys[2], rs[2];
             for (int hb = 0; hb < 2; ++hb) {
@@ -545,7 +549,13 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
             l_r0 = rs[0];
             l_r1 = rs[1];
         };
+        // the first batch's cache rows are fetched while the range's first group loads
         fetch(0);
+        {
+            TileCursor c0;
+            c0.init(prefix, p.num_groups, tb, te);
+            load_group(c0.g, 0);
+        }
         finish();
         while (ok && it < ntile) {
             const int nb = min(kBatch, ntile - it);
