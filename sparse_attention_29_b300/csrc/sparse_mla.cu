@@ -259,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tp.Lmax = p.Lmax;
         tp.k = p.k;
         tk::topk_row(tp, row, p.splits, p.cluster ? cluster_rank() : 0u, p.topk_slice, tiles);
-        __threadfence();
+        // the barrier (arrive.release / wait.acquire at cluster scope, or the CTA barrier)
+        // orders the index-set stores, global ones included, before the reads below
         if (p.cluster) cluster_sync();
         else __syncthreads();
     }
@@ -709,7 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         tc_fence_before();
-        __threadfence();
+        // release/acquire at cluster scope: the partials' global stores are visible to the
+        // peers' reads after it
         cluster_sync();  // every split's O, maxima and sums are in the workspace
         float *wts = (float *)(smem + L.wts);  // [split][head] weights
         const int ds = ((p.d + p.splits - 1) / p.splits + 7) & ~7;
