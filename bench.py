@@ -616,6 +616,8 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "value_scope": ("rank 0 alone: the oracle on this host's cores; the other ranks "
+                            "do no work, so the value does not grow with n_gpus"),
             "config": {"workload": args.workload + ": " + WORKLOADS[args.workload]},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
