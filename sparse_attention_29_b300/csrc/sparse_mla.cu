@@ -605,37 +605,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 0) *have_o_sm = have_o ? 1 : 0;
             tc_fence_before();
         } else if (p.splits == 1) {
-            uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
-            for (int mb = 0; mb < nmb; ++mb) {
-                const int dim = mb * 128 + kl;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    if (have_o) {
-                        tmem_ld32(tO + lane_addr + mb * kHeads + half * 32, v);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = 0u;
-                    }
-                    if (dim < p.d) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int h = half * 32 + e;
-                            if (h < p.H) {
-                                const float l = lsum[h];
-                                const float o = l > 0.f ? __uint_as_float(v[e]) / l : 0.f;
-                                out[(int64_t)h * p.d + dim] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-                            }
-                        }
-                    }
-                }
-            }
-            if (kl < p.H && p.lse[layer]) {
+            // the row is complete: its log-sum-exp and 1 / l (into alpha, free now) here,
+            // the output below by all warps
+            if (tid == 0) *have_o_sm = have_o ? 1 : 0;
+            if (kl < kHeads) {
                 const float l = lsum[kl];
-                p.lse[layer][(int64_t)row * p.H + kl] =
-                    l > 0.f ? (rn[kl] * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                alpha[kl] = (have_o && l > 0.f) ? 1.f / l : 0.f;
+                if (kl < p.H && p.lse[layer])
+                    p.lse[layer][(int64_t)row * p.H + kl] =
+                        l > 0.f ? (rn[kl] * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
+            tc_fence_before();
         } else {
             // unnormalised partial: O [64][d], then R [64] (raw logit units), l [64]
             float *part = p.partial + ((int64_t)unit_out * p.splits + split) * (size_t)(kHeads * p.d + 2 * kHeads);
@@ -664,6 +644,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         asm volatile("setmaxnreg.dec.sync.aligned.u32 128;\n" ::: "memory");
+    }
+
+    if (!p.cluster && p.splits == 1) {
+        // ===== one split: the output, O / l, from tensor memory by all 16 warps =====
+        // warp w reads TMEM lanes 32 (w % 4) .. +31 (latent dims) and columns 16 (w / 4)
+        // .. +15 (heads); consecutive threads store consecutive dims of a head
+        __syncthreads();  // the softmax warps have seen O complete; 1 / l in alpha
+        tc_fence_after();
+        const bool valid_o = *have_o_sm != 0;
+        const int q = warp & 3, cg = warp >> 2;
+        const float *inv = alpha + 16 * cg;  // 1 / l of each head, 0 for an empty row
+        uint16_t *out = p.out[layer] + (int64_t)row * p.H * p.d;
+#pragma unroll 1
+        for (int mb = 0; mb < nmb; ++mb) {
+            uint32_t v[16];
+            if (valid_o) {
+                tmem_ld16(tO + ((uint32_t)(32 * q) << 16) + mb * kHeads + 16 * cg, v);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = 0u;
+            }
+            const int dim = mb * 128 + 32 * q + lane;
+            if (dim < p.d) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int h = 16 * cg + e;
+                    const float o = __uint_as_float(v[e]) * inv[e];
+                    if (h < p.H) out[(int64_t)h * p.d + dim] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+                }
+            }
+        }
     }
 
     if (p.cluster) {
