@@ -31,6 +31,13 @@
  *   - Query rows are grouped by sequence: with T rows per sequence, rows b*T .. b*T+T-1
  *     belong to sequence b.  Row t sits at position q_pos[t] and sees tokens
  *     0 .. q_pos[t] (causal; the query's own token is already cached).
+ *   - Kernels launch with programmatic dependent launch: each may start while the
+ *     previous kernel of the stream finishes.  Before it waits for that kernel
+ *     (griddepcontrol.wait) a kernel reads only the call's per-step inputs -- queries,
+ *     weights, positions, the cache layout -- never the caches, scores or index sets,
+ *     which it reads after the wait.  So per-step inputs must be complete when the call
+ *     is made: written by a copy, or by a kernel that does not trigger its dependents
+ *     early (every kernel that does not use programmatic dependent launch).
  *   - The library holds no state beyond the device error word, the kernel attributes it
  *     sets once per device and the static scratch of dsa_sparse_mla_decode_noalloc;
  *     calls on different streams with different output and workspace buffers may run
