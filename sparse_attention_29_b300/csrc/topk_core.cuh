@@ -33,7 +33,7 @@ namespace tk {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kCandCap = 2048;  // candidates ranked directly (per row, all slices)
+constexpr int kCandCap = 1024;  // candidates ranked directly (per row, all slices)
 constexpr int kMaxCluster = 8;
 
 // ---- shared memory --------------------------------------------------------------------
