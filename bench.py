@@ -485,6 +485,7 @@ def measure_hisparse(lay, dev, hbm_peak, C=4096, reps=10):
 
     mla_pool = mla_ms(pool.view(torch.bfloat16), layout)
     mla_full = mla_ms(c.kv[0], lay.layout)
+    overlap = measure_layer_overlap(lay, dev, host_kv, idx, C=C, reps=reps)
     st, code = capi.dsa_device_error()
     med = lambda x: sorted(x)[len(x) // 2]  # noqa: E731
     cold_bytes = B * k * D * 2
@@ -496,8 +497,76 @@ def measure_hisparse(lay, dev, hbm_peak, C=4096, reps=10):
             "host_link_gbs_cold": cold_bytes / (med(cold) * 1e-3) / 1e9,
             "sparse_mla_us": {"through_working_set": mla_pool * 1e3, "full_device_cache": mla_full * 1e3},
             "device_bytes": {"working_set": B * C * D * 2, "full_cache": c.n_phys * D * 2},
+            "layer_ahead_overlap": overlap,
             "device_check": "ok" if st == capi.DSA_OK else f"code {code:#x}",
             "timing": "CUDA events around single launches, median of %d" % reps}
+
+
+def measure_layer_overlap(lay, dev, host_kv, idx, C, reps, L=4, frac_new=0.05):
+    """The host tier's layer-wise overlap on an IndexShare group of L layers over the decode
+    batch (each layer with its own working set; the timing does not depend on the rows'
+    contents, so the layers share one pinned history): a decode step whose shared
+    selection differs from the previous step's in `frac_new` of each row, run with every
+    layer's fetch before its attention on one stream, and with the fetches on a second
+    stream so that layer l + 1's fetch runs while layer l attends."""
+    import torch
+    from sparse_attention_29_b300.pipeline import HostTierGroup
+    c = lay.case
+    B, k, Lmax = c.B, c.k, c.Lmax
+    idx2 = idx.clone()
+    n_new = int(k * frac_new)
+    for b in range(B):
+        row = idx[b]
+        free = torch.ones(Lmax, dtype=torch.bool, device=dev)
+        free[row[row >= 0].long()] = False
+        free[c.lengths[b]:] = False
+        cand = torch.nonzero(free).flatten()
+        new = cand[torch.randperm(cand.numel(), device=dev)[:n_new]].to(torch.int32)
+        keep = row[torch.randperm(k, device=dev)[: k - n_new]]
+        idx2[b] = torch.sort(torch.cat([keep, new])).values
+    grp = HostTierGroup([host_kv] * L, c.seq_start, B, Lmax, c.D, C, device=dev)
+    outs = [torch.empty_like(lay.out[0]) for _ in range(L)]
+    lses = [torch.empty_like(lay.lse[0]) for _ in range(L)]
+    qs = [c.q[0]] * L
+    args = (c.H, c.d, c.r, c.softmax_scale, lay.workspace, lay.ws_bytes)
+
+    def step_ms(overlap):
+        times = []
+        for _ in range(reps):
+            grp.reset()
+            grp.step(idx, k, 1, qs, outs, lses, *args, overlap=overlap)  # the previous step
+            torch.cuda.synchronize()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            grp.step(idx2, k, 2, qs, outs, lses, *args, overlap=overlap)
+            e.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(e))
+        return sorted(times)[len(times) // 2]
+
+    def one_ms(fn):
+        times = []
+        for _ in range(reps):
+            grp.reset()
+            grp.step(idx, k, 1, qs, outs, lses, *args, overlap=False)
+            torch.cuda.synchronize()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(e))
+        return sorted(times)[len(times) // 2]
+
+    seq = step_ms(False)
+    ov = step_ms(True)
+    fetch = one_ms(lambda: grp.fetch(0, idx2, k, 2))
+    misses = int(grp.stats[0][:, 1].sum().item())  # of that fetch
+    mla = one_ms(lambda: grp.mla(0, idx, k, qs[0], outs[0], lses[0], *args))
+    return {"layers": L, "selection_new_per_row": n_new,
+            "step_us": {"fetch_then_attend": seq * 1e3, "layer_ahead_overlap": ov * 1e3},
+            "per_layer_us": {"fetch": fetch * 1e3, "sparse_mla": mla * 1e3},
+            "rows_fetched_per_layer": misses}
 
 
 def measure_mha_vs_mqa(dev, contexts=(2048, 4096, 8192), T=1024, H=64, reps=5):

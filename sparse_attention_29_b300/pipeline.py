@@ -115,3 +115,73 @@ class DsaLayer:
         st, code = libdsa.dsa_device_error(self.stream)
         if st != libdsa.DSA_OK:
             raise libdsa.DsaError(f"device check (code {code:#x})", st)
+
+
+class HostTierGroup:
+    """The latent caches of an IndexShare group behind the host tier.
+
+    Per layer the full history stays in pinned host memory and the device keeps a working
+    set of C slots per sequence, least recently used (dsa_hisparse_init / _fetch); the
+    sparse MLA reads a layer's working set as a cache of one-token pages.  step() runs one
+    decode step of the group over its shared index set: each layer's fetch, then its sparse
+    MLA.  With `overlap`, the fetches run in order on a second stream and layer l + 1's
+    fetch proceeds while layer l attends (the host tier's layer-wise overlap); a layer's
+    MLA waits only for its own fetch, and a step's fetches wait for the previous step's
+    attention, which still reads the slots they refill.
+
+        group = HostTierGroup(host_kv_layers, host_seq_start, B, Lmax, D, C)
+        group.reset()
+        group.step(idx, k, step_no, q_layers, out_layers, lse_layers, H, d, r, scale,
+                   workspace, ws_bytes)
+    """
+
+    def __init__(self, host_kv_layers, host_seq_start, B, Lmax, D, C, device="cuda"):
+        self.host_kv = list(host_kv_layers)  # pinned host tensors [rows, D] of bf16 bits
+        self.host_seq_start = host_seq_start  # device int32 [B]: first host row of each sequence
+        self.B, self.Lmax, self.D, self.C = B, Lmax, D, C
+        L = len(self.host_kv)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.res = [torch.empty((B, Lmax), **i32) for _ in range(L)]
+        self.stok = [torch.empty((B, C), **i32) for _ in range(L)]
+        self.use = [torch.empty((B, C), **i32) for _ in range(L)]
+        self.pool = [torch.empty((B * C, D), dtype=torch.int16, device=device) for _ in range(L)]
+        self.stats = [torch.zeros((B, 2), **i32) for _ in range(L)]
+        self.layouts = [libdsa.make_layout(B * C, block_table=r, page_size=1) for r in self.res]
+        self.fetch_stream = torch.cuda.Stream(device=device)
+        self.fetched = [torch.cuda.Event() for _ in range(L)]
+
+    def reset(self):
+        for g in range(len(self.host_kv)):
+            libdsa.dsa_hisparse_init(self.res[g], self.B, self.Lmax, self.stok[g], self.use[g],
+                                     self.C)
+
+    def fetch(self, g, idx, k, step_no, stream=None):
+        libdsa.dsa_hisparse_fetch(idx, self.B, k, step_no, self.host_kv[g], self.host_seq_start,
+                                  self.D, self.res[g], self.Lmax, self.stok[g], self.use[g],
+                                  self.C, self.pool[g], self.stats[g], stream)
+
+    def mla(self, g, idx, k, q, out, lse, H, d, r, scale, workspace, ws_bytes, stream=None):
+        libdsa.dsa_sparse_mla_decode(q, self.pool[g].view(torch.bfloat16), self.layouts[g], idx,
+                                     self.B, H, d, r, k, scale, out, lse, workspace, ws_bytes,
+                                     stream)
+
+    def step(self, idx, k, step_no, q_layers, out_layers, lse_layers, H, d, r, scale,
+             workspace, ws_bytes, overlap=True):
+        L = len(self.host_kv)
+        main = torch.cuda.current_stream()
+        if not overlap:
+            for g in range(L):
+                self.fetch(g, idx, k, step_no)
+                self.mla(g, idx, k, q_layers[g], out_layers[g], lse_layers[g], H, d, r, scale,
+                         workspace, ws_bytes)
+            return
+        fs = self.fetch_stream
+        fs.wait_stream(main)  # the previous step's attention is done with the slots
+        for g in range(L):
+            self.fetch(g, idx, k, step_no, fs.cuda_stream)
+            self.fetched[g].record(fs)
+        for g in range(L):
+            main.wait_event(self.fetched[g])
+            self.mla(g, idx, k, q_layers[g], out_layers[g], lse_layers[g], H, d, r, scale,
+                     workspace, ws_bytes)
+        main.wait_stream(fs)

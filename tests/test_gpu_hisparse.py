@@ -99,3 +99,49 @@ def test_working_set_matches_oracle_and_attention_is_unchanged(lengths, C, k):
         torch.cuda.synchronize()
         assert capi.dsa_device_error()[0] == capi.DSA_OK
         assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1]), step
+
+
+def test_layer_ahead_overlap_equals_sequential_and_full_cache():
+    """An IndexShare group of 3 layers behind the host tier, 3 decode steps: with the
+    fetches on a second stream (layer l + 1's fetch while layer l attends) every layer's
+    output and log-sum-exp equal those of the one-stream schedule and of the sparse MLA
+    over the full device cache, bit for bit."""
+    from sparse_attention_29_b300.pipeline import HostTierGroup
+    case = inputs.make_case(seed=85, lengths=[5000, 3000, 4200], T=1, layers=3, k=512)
+    B, D, Lmax, k, L, C = case.B, case.D, case.Lmax, case.k, case.layers, 1024
+    dev = "cuda"
+    full = case.to(dev)
+    host = [case.kv[g].view(torch.int16).pin_memory() for g in range(L)]
+    host_start = case.seq_start.to(dev)
+    full_layout = capi.make_layout(full.n_phys, seq_start=full.seq_start)
+    ws = capi.dsa_workspace_bytes(capi.DSA_OP_SPARSE_MLA, B, 1, case.H, case.d, k, 1)
+    w = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+
+    def buffers():
+        return ([torch.empty((B, case.H, case.d), dtype=torch.bfloat16, device=dev) for _ in range(L)],
+                [torch.empty((B, case.H), dtype=torch.float32, device=dev) for _ in range(L)])
+
+    sel = [torch.from_numpy(r).to(dev) for r in selections(case.lengths, k, 3, seed=9)]
+    results = {}
+    for overlap in (False, True):
+        grp = HostTierGroup(host, host_start, B, Lmax, D, C)
+        grp.reset()
+        per_step = []
+        for s, idx in enumerate(sel, start=1):
+            out, lse = buffers()
+            grp.step(idx, k, s, full.q, out, lse, case.H, case.d, case.r, case.softmax_scale,
+                     w, ws, overlap=overlap)
+            torch.cuda.synchronize()
+            assert capi.dsa_device_error()[0] == capi.DSA_OK
+            per_step.append(([o.clone() for o in out], [x.clone() for x in lse]))
+        results[overlap] = per_step
+    for s, idx in enumerate(sel):
+        ref_out, ref_lse = buffers()
+        for g in range(L):
+            capi.dsa_sparse_mla_decode(full.q[g], full.kv[g], full_layout, idx, B, case.H, case.d,
+                                       case.r, k, case.softmax_scale, ref_out[g], ref_lse[g], w, ws)
+        torch.cuda.synchronize()
+        for g in range(L):
+            for ov in (False, True):
+                assert torch.equal(results[ov][s][0][g], ref_out[g]), (s, g, ov)
+                assert torch.equal(results[ov][s][1][g], ref_lse[g]), (s, g, ov)
