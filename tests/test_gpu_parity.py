@@ -141,6 +141,34 @@ def test_sparse_mla_matches_oracle(lengths, T, k, paged):
     check_mla(lay.out[0], lay.lse[0], ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("k", [1, 33, 4096, 8192])
+def test_topk_and_mla_edge_k(k):
+    """k at the ends of the supported range: one key, a partial tile, and 64 / 128 tiles
+    (a row then needs more splits' worth of tiles); a sparse and a dense row.  The index
+    set from the GPU's own top-k equals the oracle's (scores fixed by the oracle), the
+    attention matches the oracle fed it, and the one-call form equals the two calls."""
+    case = inputs.make_case(seed=500 + k, lengths=[12000, 300, 9000], T=1, k=k)
+    lay = gpu_layer(case)
+    lay.indexer()
+    lay.topk()
+    lay.mla()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref_scores = oracle.indexer_scores(case)
+    check_topk_sets(lay.idx, ref_scores, case.q_pos, case.k)
+    gidx = cpu(lay.idx)
+    ref_out, ref_lse = oracle.sparse_mla(case, gidx)
+    check_mla(lay.out[0], lay.lse[0], ref_out, ref_lse)
+    idx_sep, out_sep, lse_sep = lay.idx.clone(), lay.out[0].clone(), lay.lse[0].clone()
+    lay.idx.fill_(-7)
+    lay.out[0].zero_()
+    lay.topk_mla()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    assert torch.equal(lay.idx, idx_sep)
+    assert torch.equal(lay.out[0], out_sep) and torch.equal(lay.lse[0], lse_sep)
+
+
 def test_sparse_mla_small_heads_and_dims():
     case = inputs.make_case(seed=9, lengths=[900, 400], T=2, Hi=4, Di=32, H=12, d=128, r=32,
                             k=300, softmax_scale=0.1)
