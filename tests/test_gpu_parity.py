@@ -268,3 +268,31 @@ def test_topk_and_mla_in_one_call_equal_the_two_calls(lengths):
     assert_no_device_error(lay)
     assert torch.equal(lay.idx, idx_sep)
     assert torch.equal(lay.out[0], out_sep) and torch.equal(lay.lse[0], lse_sep)
+
+
+def test_concurrent_streams_equal_sequential_runs():
+    """Calls on different streams with their own buffers may run at once: three layers (a
+    decode batch in one call, a decode batch as two calls, a prefill chunk) stepped
+    concurrently on three streams, several times, give what each gives alone."""
+    cases = [inputs.make_case(seed=601, lengths=[3000] * 8, T=1),
+             inputs.make_case(seed=602, lengths=[5000, 2600, 900], T=1),
+             inputs.make_case(seed=603, lengths=[2500], T=16)]
+    steps = [lambda l: l.run(), lambda l: (l.indexer(), l.topk(), l.mla()), lambda l: l.run()]
+    alone = []
+    for c, st in zip(cases, steps):
+        lay = gpu_layer(c)
+        st(lay)
+        torch.cuda.synchronize()
+        assert_no_device_error(lay)
+        alone.append((lay.idx.clone(), lay.out[0].clone(), lay.lse[0].clone()))
+    streams = [torch.cuda.Stream() for _ in cases]
+    lays = [DsaLayer(c.to("cuda"), stream=s) for c, s in zip(cases, streams)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for lay, st in zip(lays, steps):
+            st(lay)
+        torch.cuda.synchronize()
+        for lay, (idx, out, lse) in zip(lays, alone):
+            assert_no_device_error(lay)
+            assert torch.equal(lay.idx, idx)
+            assert torch.equal(lay.out[0], out) and torch.equal(lay.lse[0], lse)
