@@ -117,11 +117,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete.  Returns false (and records an
-// error, and raises *abort_flag so that the other roles of the CTA stop too) if it does
-// not complete within the time limit or if another role already gave up.  Waiting
-// threads are suspended in hardware between checks instead of spinning, so that they
-// leave issue slots to the warps that do the work.
+// Non-blocking check of whether the phase of parity `parity` has completed.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -134,6 +130,11 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Wait for the phase of parity `parity` to complete.  Returns false (and records an
+// error, and raises *abort_flag so that the other roles of the CTA stop too) if it does
+// not complete within the time limit or if another role already gave up.  Waiting
+// threads are suspended in hardware between checks instead of spinning, so that they
+// leave issue slots to the warps that do the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int kid,
                                           volatile int *abort_flag) {
     if (mbar_test(bar, parity)) return true;  // cheap non-blocking check first
@@ -164,20 +165,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-
-// Gather four rows (y0..y3) of a 2D tensor, each `box width` elements wide starting at
-// column x, into four consecutive box rows in shared memory.  The tensor map's box must be
-// one row high.  x must be a multiple of 16 bytes.
-__device__ __forceinline__ void tma_gather4(void *smem_dst, const CUtensorMap *map,
-                                            uint64_t *bar, int x, int y0, int y1, int y2,
-                                            int y3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1),
-        "r"(y2), "r"(y3)
         : "memory");
 }
 
@@ -489,8 +476,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // ---------------------------------------------------------------------------------
 // misc
-
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
