@@ -70,6 +70,72 @@ def scores_in_step(case):
     return sum(8 * (L - case.T + 1 + i) for L in case.lengths for i in range(case.T))
 
 
+def one_call_bytes(case):
+    """Algorithmic bytes of the one-call top-k + sparse MLA launch: the scores read and the
+    index set written once (the kernel reads its own index set back from L2), plus the
+    sparse MLA's selected rows, query and output."""
+    _, b_topk, b_mla = per_query_bytes(case)
+    return b_topk + b_mla - 4 * case.k * case.rows
+
+
+IDX_FILES = ["sparse_attention_29_b300/csrc/indexer.cu", "sparse_attention_29_b300/csrc/ptx.cuh"]
+MLA_FILES = ["sparse_attention_29_b300/csrc/sparse_mla.cu", "sparse_attention_29_b300/csrc/ptx.cuh",
+             "sparse_attention_29_b300/csrc/topk_core.cuh", "sparse_attention_29_b300/csrc/keys.cuh"]
+TOPK_FILES = ["sparse_attention_29_b300/csrc/topk.cu", "sparse_attention_29_b300/csrc/topk_core.cuh",
+              "sparse_attention_29_b300/csrc/ptx.cuh", "sparse_attention_29_b300/csrc/keys.cuh"]
+
+
+def step_rooflines(case, args, k_idx, k_topk, k_mla, k_fused, shared, hbm_peak, bf16_peak,
+                   peak_src):
+    """The roofline of every kernel of the step (warm per-launch times), and that of the
+    kernel with the largest share of the step's kernel time, which is the headline one.
+
+    Decode: each kernel against the measured copy bandwidth, with its algorithmic bytes.
+    Chunked prefill: the indexer against the fp8 tensor peak (the measured bf16 burst peak
+    x 2, the nominal fp8:bf16 ratio), over the q.k dot products of every visible key; the
+    sparse MLA against the bf16 peak, over its two products per selected key; the top-k
+    against the copy bandwidth."""
+    b_idx, b_topk, b_mla = per_query_bytes(case)
+    wl = args.workload
+
+    def hbm(name, nbytes, ms, traffic=None):
+        ach = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": hbm_peak,
+                "unit": "GB/s", "frac": ach / hbm_peak, "traffic": traffic,
+                "algorithmic_bytes": nbytes, "ms": ms, "peak_source": peak_src}
+
+    def tensor(name, flops, ms, peak, src):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": name, "achieved": tf, "peak": peak,
+                "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                "algorithmic_flops": flops, "ms": ms, "peak_source": src}
+
+    out = {}
+    if case.T > 1:
+        pos = case.q_pos.long().add(1)
+        flops = float(pos.sum().item()) * case.Hi * case.Di * 2.0
+        out["indexer"] = tensor("indexer", flops, k_idx, 2.0 * bf16_peak,
+                                f"{peak_src} bf16 burst x 2 (nominal fp8:bf16 ratio)")
+        out["topk"] = hbm("topk", b_topk, k_topk)
+        nsel = float(pos.clamp(max=case.k).sum().item()) * case.layers
+        mla_flops = nsel * case.H * (2.0 * (case.d + case.r) + 2.0 * case.d)
+        out["sparse_mla"] = tensor("sparse_mla", mla_flops, k_mla, bf16_peak,
+                                   f"{peak_src} bf16 burst")
+    else:
+        out["indexer"] = hbm("indexer", b_idx, k_idx, traffic_for(IDX_FILES, "indexer", wl))
+        if k_fused:
+            out["topk_and_sparse_mla_one_call"] = hbm(
+                "topk_and_sparse_mla_one_call", one_call_bytes(case), k_fused,
+                traffic_for(MLA_FILES, "sparse_mla", wl))
+        else:
+            out["topk"] = hbm("topk", b_topk, k_topk, traffic_for(TOPK_FILES, "topk", wl))
+            out["sparse_mla_shared" if shared else "sparse_mla"] = hbm(
+                "sparse_mla_shared" if shared else "sparse_mla", b_mla, k_mla)
+    timed = [r for r in out.values() if r["ms"] == r["ms"]]  # NaN in a profile run
+    head = max(timed, key=lambda r: r["ms"]) if timed else out["indexer"]
+    return head, out
+
+
 def src_sha(files):
     h = hashlib.sha256()
     for f in files:
@@ -1055,24 +1121,8 @@ def main():
         return 0
 
     hbm_peak, bf16_peak, peak_src = load_peaks()
-    idx_files = ["sparse_attention_29_b300/csrc/indexer.cu", "sparse_attention_29_b300/csrc/ptx.cuh"]
-    achieved = b_idx / (k_idx * 1e-3) / 1e9
-    roof = {"bound": "hbm", "kernel": "indexer", "achieved": achieved,
-            "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-            "traffic": traffic_for(idx_files, "indexer", args.workload),
-            "algorithmic_bytes": b_idx, "peak_source": peak_src}
-    if case.T > 1:
-        # several query rows per sequence (chunked prefill): the indexer is a dense fp8
-        # contraction, so its roofline is the fp8 tensor peak (the measured bf16 burst
-        # peak x 2, the nominal fp8:bf16 ratio); algorithmic FLOPs are the q.k dot products
-        # over every visible key: sum over rows of (q_pos + 1) x Hi x Di x 2
-        flops = float(case.q_pos.long().add(1).sum().item()) * case.Hi * case.Di * 2.0
-        fp8_peak = 2.0 * bf16_peak
-        tflops = flops / (k_idx * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "indexer", "achieved": tflops, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": tflops / fp8_peak, "traffic": None,
-                "algorithmic_flops": flops,
-                "peak_source": f"{peak_src} bf16 burst x 2 (nominal fp8:bf16 ratio)"}
+    roof, rooflines = step_rooflines(case, args, k_idx, k_topk, k_mla, k_fused, shared,
+                                     hbm_peak, bf16_peak, peak_src)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -1096,6 +1146,7 @@ def main():
         "kernel_ms": {"indexer": k_idx, "topk": k_topk, "sparse_mla": k_mla,
                       **({"topk_and_sparse_mla_one_call": k_fused} if k_fused else {})},
         "roofline": roof,
+        "rooflines": rooflines,
         "gpu_launches": launches_per_step * args.steps,
         "graph_replay": (graph_ms if isinstance(graph_ms, str) else
                          {"ms_per_step": graph_ms,
