@@ -810,7 +810,35 @@ __global__ void __launch_bounds__(EpiCfg<kW64>::kThreads, 1)
                 } else {
                     // both sets work on every tile: set e takes query rows e, e + 2, ...
                     const float *wq = wbuf + slot * p.N;
-                    if (kSel || p.HP == 64) {  // the fused selection runs 64-head rows only
+                    if (!kSel && p.HP == 64 && eset + kEpiSets < nr) {
+                        // this set's two rows (64 heads: at most 256 / 64 = 4 rows per group)
+                        // together: both rows' 64-column loads, one wait, then the two rows'
+                        // sums interleaved, each row's chains as in the one-row loop below
+                        // (twice the independent work per wait: prefill_8k 7.41 -> 6.73 ms;
+                        // with fused selection it spilled and was slower)
+                        const int qa = eset, qb = eset + kEpiSets;
+                        uint32_t va[64], vb[64];
+                        tmem_ld32(tacc + (uint32_t)(qa * 64), *reinterpret_cast<uint32_t (*)[32]>(&va[0]));
+                        tmem_ld32(tacc + (uint32_t)(qa * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&va[32]));
+                        tmem_ld32(tacc + (uint32_t)(qb * 64), *reinterpret_cast<uint32_t (*)[32]>(&vb[0]));
+                        tmem_ld32(tacc + (uint32_t)(qb * 64 + 32), *reinterpret_cast<uint32_t (*)[32]>(&vb[32]));
+                        tmem_ld_wait();
+                        const ulonglong2 *wa = reinterpret_cast<const ulonglong2 *>(wq + qa * 64);
+                        const ulonglong2 *wb = reinterpret_cast<const ulonglong2 *>(wq + qb * 64);
+                        uint64_t a01 = 0, a23 = 0, b01 = 0, b23 = 0;
+#pragma unroll
+                        for (int h = 0; h < 64; h += 4) {
+                            const ulonglong2 x = wa[h >> 2], y = wb[h >> 2];
+                            a01 = fma2(x.x, relu2(va[h + 0], va[h + 1]), a01);
+                            a23 = fma2(x.y, relu2(va[h + 2], va[h + 3]), a23);
+                            b01 = fma2(y.x, relu2(vb[h + 0], vb[h + 1]), b01);
+                            b23 = fma2(y.y, relu2(vb[h + 2], vb[h + 3]), b23);
+                        }
+                        const float sa = (sum2(a01) + sum2(a23)) * ksc;
+                        const float sb = (sum2(b01) + sum2(b23)) * ksc;
+                        if (s <= pos[qa]) p.scores[(int64_t)(r0 + qa) * p.Lmax + s] = sa;
+                        if (s <= pos[qb]) p.scores[(int64_t)(r0 + qb) * p.Lmax + s] = sb;
+                    } else if (kSel || p.HP == 64) {  // the fused selection runs 64-head rows only
                         // this set's rows one at a time: one 64-column load and wait each
                         for (int q = eset; q < nr; q += kEpiSets) {
                             // fused selection: this row's threshold for the tile, and whether
