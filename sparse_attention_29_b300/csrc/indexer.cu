@@ -113,16 +113,12 @@ __device__ __forceinline__ uint32_t swz_off(int row, int gran, int pitch) {
     return lin ^ (((lin >> 7) & mask) << 4);
 }
 
+// The query group and in-group index of tile t0 of the list of all (group, key tile) pairs.
 struct TileCursor {
-    const int *prefix;
-    int num_groups;
-    int g, j, t, te;
-    __device__ void init(const int *pre, int ng, int t0, int te_) {
-        prefix = pre;
-        num_groups = ng;
+    int g, j, t;
+    __device__ void init(const int *pre, int ng, int t0, int te) {
         t = t0;
-        te = te_;
-        if (t0 >= te_) {
+        if (t0 >= te) {
             g = ng;
             j = 0;
             return;
@@ -137,18 +133,7 @@ struct TileCursor {
         g = lo;
         j = t0 - pre[g];
     }
-    __device__ bool valid() const { return t < te; }
-    __device__ int tiles_in_group() const { return prefix[g + 1] - prefix[g]; }
     __device__ bool first_in_range(int tb) const { return j == 0 || t == tb; }
-    __device__ bool last_in_range() const { return j == tiles_in_group() - 1 || t == te - 1; }
-    __device__ void next() {
-        ++t;
-        ++j;
-        while (g < num_groups && j >= prefix[g + 1] - prefix[g]) {
-            ++g;
-            j = 0;
-        }
-    }
 };
 
 // Walks the groups of a CTA's tile range [tb, tb + n) in order: `g` is the group of the
