@@ -169,6 +169,27 @@ def test_topk_and_mla_edge_k(k):
     assert torch.equal(lay.out[0], out_sep) and torch.equal(lay.lse[0], lse_sep)
 
 
+@pytest.mark.parametrize("H,d,r,T", [
+    (32, 256, 0, 1),    # no rope dims: the key is the latent part alone
+    (64, 448, 64, 1),   # seven latent chunks: the last value M-block is half used
+    (16, 384, 32, 3),   # prefill form, six latent chunks, 16 heads
+    (48, 192, 8, 1),    # three latent chunks, a rope part one 16-byte granule wide
+])
+def test_sparse_mla_other_shapes(H, d, r, T):
+    """Shapes inside the supported range (H <= 64, d a multiple of 64 up to 512, r <= 64)
+    that the production and tiny cases do not reach, decode (split-KV) and prefill, with
+    2 % invalid indices, against the oracle fed the same index set."""
+    case = inputs.make_case(seed=700 + d + r, lengths=[3000, 900], T=T, Hi=4, Di=32, H=H,
+                            d=d, r=r, k=512)
+    lay = gpu_layer(case)
+    idx = _random_idx(case, seed=d + r, frac_invalid=0.02)
+    lay.mla(idx=idx.cuda())
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref_out, ref_lse = oracle.sparse_mla(case, idx)
+    check_mla(lay.out[0], lay.lse[0], ref_out, ref_lse)
+
+
 def test_sparse_mla_small_heads_and_dims():
     case = inputs.make_case(seed=9, lengths=[900, 400], T=2, Hi=4, Di=32, H=12, d=128, r=32,
                             k=300, softmax_scale=0.1)
