@@ -66,6 +66,25 @@ def test_indexer_matches_oracle(lengths, T, paged):
     check_case_scores(lay.scores, case)
 
 
+@pytest.mark.parametrize("Hi,Di,T", [
+    (128, 128, 1),   # decode, 128 heads: one row of N = 128 per tile
+    (128, 128, 5),   # two rows of 128 heads per tile, a ragged last group
+    (256, 64, 2),    # the widest query group: one row of N = 256
+    (100, 128, 3),   # heads padded to 112, two rows per tile
+    (1, 32, 20),     # one head padded to 16: sixteen rows per tile
+])
+def test_indexer_wide_and_narrow_heads(Hi, Di, T):
+    """Head counts away from 64 (up to the 256 columns of one tensor-core tile), where the
+    epilogue takes the general path, in decode and prefill form, against the oracle."""
+    case = inputs.make_case(seed=31 + Hi + T, lengths=[1500, 777], T=T, Hi=Hi, Di=Di, H=4,
+                            d=64, r=16, k=256)
+    lay = gpu_layer(case)
+    lay.indexer()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    check_case_scores(lay.scores, case)
+
+
 @pytest.mark.parametrize("Hi,Di", [(4, 32), (16, 64), (24, 128), (64, 32)])
 def test_indexer_head_shapes(Hi, Di):
     case = inputs.make_case(seed=7 + Hi, lengths=[1000, 301], T=3, Hi=Hi, Di=Di, H=4, d=64,
