@@ -126,6 +126,31 @@ def test_topk_exact_on_fixed_scores(Lmax, k, levels):
     assert np.array_equal(cpu(out).numpy(), ref)
 
 
+def test_topk_exact_on_extreme_scores():
+    """Scores the fp16-based bins cannot separate: beyond the fp16 range (every one in the
+    infinity bin), +inf and -inf runs, subnormals (all in the zero bin with +-0), and
+    distinct fp32 values inside one fp16 step; the selection stays exact, ties to the
+    lower index."""
+    Lmax, k, rows = 20000, 2048, 6
+    g = torch.Generator().manual_seed(77)
+    s = torch.randn((rows, Lmax), generator=g)
+    s[0] *= 1e30                                   # beyond fp16: one bin holds all
+    s[1, torch.randperm(Lmax, generator=g)[:100]] = float("inf")
+    s[2] *= 1e-40                                  # subnormal: the zero bin, with +-0
+    s[2, 10:20] = 0.0
+    s[2, 20:30] = -0.0
+    s[3, torch.randperm(Lmax, generator=g)[: Lmax // 2]] = float("-inf")
+    s[4] = 1.0 + torch.arange(Lmax, dtype=torch.float32) * 2.0 ** -20  # one fp16 step wide
+    s[4, ::7] = 1.0 + 2.0 ** -20 * 19990              # and ~2900 exact ties near the top
+    q_pos = torch.full((rows,), Lmax - 1, dtype=torch.int32)
+    q_pos[5] = Lmax // 3
+    out = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    capi.dsa_topk(s.cuda(), q_pos.cuda(), rows, Lmax, k, out)
+    torch.cuda.synchronize()
+    ref = oracle.topk(s.numpy(), q_pos.numpy(), k)
+    assert np.array_equal(cpu(out).numpy(), ref)
+
+
 # ---- sparse MLA ---------------------------------------------------------------------------
 
 def _random_idx(case, seed, frac_invalid=0.0):
