@@ -335,6 +335,38 @@ def test_topk_and_mla_in_one_call_equal_the_two_calls(lengths):
     assert torch.equal(lay.out[0], out_sep) and torch.equal(lay.lse[0], lse_sep)
 
 
+def test_one_call_on_extreme_scores():
+    """The one-call decode form on scores that force the radix passes and the tie rules
+    inside the sparse MLA kernel's tile buffers: the index sets equal the oracle's, and
+    index sets and attention equal the two calls bit for bit."""
+    case = inputs.make_case(seed=88, lengths=[20000] * 6, T=1)
+    lay = gpu_layer(case)
+    g = torch.Generator().manual_seed(78)
+    s = torch.randn((6, case.Lmax), generator=g)
+    s[0] *= 1e30                                   # one fp16 bin holds half the row
+    s[1, torch.randperm(case.Lmax, generator=g)[:100]] = float("inf")
+    s[2] *= 1e-40                                  # subnormals and +-0
+    s[2, 10:20] = 0.0
+    s[2, 20:30] = -0.0
+    s[4] = 1.0 + torch.arange(case.Lmax, dtype=torch.float32) * 2.0 ** -20
+    s[4, ::7] = 1.0 + 2.0 ** -20 * 19990           # ~2900 exact ties near the top
+    lay.scores.copy_(s.cuda())
+    lay.topk()
+    lay.mla()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    ref = oracle.topk(s.numpy(), cpu(case.q_pos).numpy(), case.k)
+    assert np.array_equal(cpu(lay.idx).numpy(), ref)
+    idx_sep, out_sep, lse_sep = lay.idx.clone(), lay.out[0].clone(), lay.lse[0].clone()
+    lay.idx.fill_(-7)
+    lay.out[0].zero_()
+    lay.topk_mla()
+    torch.cuda.synchronize()
+    assert_no_device_error(lay)
+    assert torch.equal(lay.idx, idx_sep)
+    assert torch.equal(lay.out[0], out_sep) and torch.equal(lay.lse[0], lse_sep)
+
+
 def test_concurrent_streams_equal_sequential_runs():
     """Calls on different streams with their own buffers may run at once: three layers (a
     decode batch in one call, a decode batch as two calls, a prefill chunk) stepped
