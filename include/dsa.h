@@ -367,9 +367,24 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
  * Synchronises `stream`, then reads and clears the device error word.  Returns DSA_OK
  * if no device-side check fired since the last call, else DSA_ERR_DEVICE and, if `code`
  * is not NULL, the first recorded code (kernel id << 16 | reason; kernel ids: 1 indexer,
- * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append, 6 host-tier fetch, 7 MHA mode).
+ * 2 top-k, 3 sparse MLA, 4 split combine, 5 cache append, 6 host-tier fetch, 7 MHA mode,
+ * 8 wait probe; reasons: 1 a wait ran out, 2 a bad position, 3 a bad index, 4 a bad page,
+ * 5 tensor memory unavailable).
  */
 dsa_status_t dsa_device_error(void *stream, uint32_t *code);
+
+/*
+ * Diagnostics, not part of the method: checks on the device that a kernel's bounded wait
+ * ends a broken pipeline instead of hanging it.  Launches one CTA whose two waiters wait,
+ * through the same bounded wait every libdsa pipeline uses, on a barrier that nothing
+ * completes: the first gives up after the time limit (about two seconds), records
+ * (8 << 16 | 1) in the device error word and stops the other, which gives up at once.
+ * `result` (device, 8-byte aligned, 4 x uint64_t, written by the kernel): per waiter
+ * whether its barrier completed (expected 0), then how long each waited in nanoseconds.
+ * Nothing faults; afterwards dsa_device_error() returns DSA_ERR_DEVICE with that code
+ * and clears it, and the device is usable as before.
+ */
+dsa_status_t dsa_wait_probe(uint64_t *result, void *stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,8 @@ EXPORTS = ("dsa_version", "dsa_status_string", "dsa_indexer_scores", "dsa_topk",
            "dsa_sparse_mla_shared", "dsa_cache_append", "dsa_workspace_bytes",
            "dsa_device_error", "dsa_indexer_topk", "dsa_indexer_topk_workspace_bytes",
            "dsa_hisparse_init", "dsa_hisparse_fetch", "dsa_mla_up_project",
-           "dsa_mha_workspace_bytes", "dsa_sparse_mha_prefill", "dsa_topk_sparse_mla_decode")
+           "dsa_mha_workspace_bytes", "dsa_sparse_mha_prefill", "dsa_topk_sparse_mla_decode",
+           "dsa_wait_probe")
 
 
 class DsaError(RuntimeError):
@@ -97,6 +98,8 @@ def load(path: str = LIB_PATH):
     lib.dsa_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     lib.dsa_device_error.restype = I
     lib.dsa_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dsa_wait_probe.restype = I
+    lib.dsa_wait_probe.argtypes = [P, P]
     _lib = lib
     return lib
 
@@ -270,6 +273,11 @@ def dsa_sparse_mla_shared(q_layers, kv_layers, layout, idx, B, T, H, d, r, k, sc
                                       None if la is None else ctypes.cast(la, ctypes.c_void_p),
                                       _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check("dsa_sparse_mla_shared", st)
+
+
+def dsa_wait_probe(result, stream=None):
+    """Diagnostics: a bounded wait that runs out on purpose (result: 4 uint64 on the device)."""
+    _check("dsa_wait_probe", load().dsa_wait_probe(_ptr(result), _stream(stream)))
 
 
 def dsa_device_error(stream=None):

@@ -650,11 +650,18 @@ dsa_status_t dsa_sparse_mha_prefill(const uint16_t *q, const uint16_t *k_up,
     return from_cuda(launch_mha(p, qmap, kmap, rmap, vmap, idx, static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status_t dsa_wait_probe(uint64_t *result, void *stream) {
+    if (!result || (reinterpret_cast<uintptr_t>(result) & 7) != 0) return DSA_ERR_INVALID_ARG;
+    return from_cuda(launch_wait_probe(reinterpret_cast<unsigned long long *>(result),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_device_error(void *stream, uint32_t *code) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return from_cuda(cudaErrorUnknown);
-    const uint32_t words[6] = {take_error_indexer(), take_error_topk(), take_error_mla(),
-                               take_error_append(), take_error_hisparse(), take_error_mha()};
+    const uint32_t words[7] = {take_error_indexer(), take_error_topk(), take_error_mla(),
+                               take_error_append(), take_error_hisparse(), take_error_mha(),
+                               take_error_probe()};
     uint32_t first = 0;
     for (uint32_t v : words) {
         if (v == 0xFFFFFFFFu) return DSA_ERR_CUDA;

@@ -235,4 +235,8 @@ struct AppendParams {
 };
 cudaError_t launch_cache_append(const AppendParams &p, cudaStream_t stream);
 
+// ---- diagnostics: a bounded wait that runs out on purpose ---------------------------------
+cudaError_t launch_wait_probe(unsigned long long *out, cudaStream_t stream);
+uint32_t take_error_probe();
+
 }  // namespace dsa

@@ -135,3 +135,6 @@ def test_hisparse_checks_fail_before_any_launch(lib):
                                   None, None) == UNSUPPORTED
     assert lib.dsa_hisparse_init(p, 1, 100, p, p, 20000, None) == UNSUPPORTED
     assert lib.dsa_hisparse_init(None, 1, 100, p, p, 16, None) == INVALID
+    # the wait probe: a result pointer is required and must be 8-byte aligned
+    assert lib.dsa_wait_probe(None, None) == INVALID
+    assert lib.dsa_wait_probe(ctypes.c_void_p(4100), None) == INVALID
