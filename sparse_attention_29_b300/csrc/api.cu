@@ -3,6 +3,7 @@
 // Every entry point validates its arguments before it launches anything and returns a
 // dsa_status_t; no C++ exception crosses the ABI.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdio>
 #include <cstring>
@@ -16,6 +17,17 @@ using namespace dsa;
 namespace {
 
 #define DSA_VERSION_STRING "libdsa 0.1.0 (sm_103a)"
+
+// One NVTX range per C-ABI call that launches work, named after the entry point, so that
+// a timeline tool shows which call launched which kernels.  With no tool attached a range
+// costs a check of a function pointer.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
+#define DSA_CALL_RANGE() const CallRange dsa_call_range_(__func__)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -360,6 +372,7 @@ dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const f
                                 const dsa_cache_layout_t *layout, const int32_t *q_pos,
                                 int B, int T, int Hi, int Di, int Lmax, float *scores,
                                 void *stream) {
+    DSA_CALL_RANGE();
     return indexer_common(q8, q_scale, w, k8_cache, k_scale, layout, q_pos, B, T, Hi, Di, Lmax,
                           scores, 0, nullptr, 0, nullptr, stream);
 }
@@ -375,6 +388,7 @@ dsa_status_t dsa_indexer_topk(const uint8_t *q8, const float *q_scale, const flo
                               const dsa_cache_layout_t *layout, const int32_t *q_pos, int B,
                               int T, int Hi, int Di, int Lmax, int k, int32_t *idx,
                               void *workspace, size_t workspace_bytes, void *stream) {
+    DSA_CALL_RANGE();
     if (!idx || !workspace) return DSA_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || Lmax <= 0 || k <= 0) return DSA_ERR_INVALID_ARG;
     if (k > 8192) return DSA_ERR_UNSUPPORTED;
@@ -402,6 +416,7 @@ dsa_status_t dsa_indexer_topk(const uint8_t *q8, const float *q_scale, const flo
 
 dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int Lmax, int k,
                       int32_t *idx, void *stream) {
+    DSA_CALL_RANGE();
     if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
     if (rows <= 0 || Lmax <= 0 || k <= 0) return DSA_ERR_INVALID_ARG;
     if (k > 8192) return DSA_ERR_UNSUPPORTED;
@@ -422,6 +437,7 @@ dsa_status_t dsa_sparse_mla_decode(const uint16_t *q, const uint16_t *kv_cache,
                                    int B, int H, int d, int r, int k, float scale,
                                    uint16_t *out, float *lse, void *workspace,
                                    size_t workspace_bytes, void *stream) {
+    DSA_CALL_RANGE();
     return mla_common(&q, &kv_cache, 1, layout, idx, B, 1, H, d, r, k, scale, &out,
                       lse ? &lse : nullptr, workspace, workspace_bytes, stream);
 }
@@ -432,6 +448,7 @@ dsa_status_t dsa_topk_sparse_mla_decode(const float *scores, const int32_t *q_po
                                         int H, int d, int r, int k, float scale, uint16_t *out,
                                         float *lse, void *workspace, size_t workspace_bytes,
                                         void *stream) {
+    DSA_CALL_RANGE();
     if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
     if (Lmax <= 0) return DSA_ERR_INVALID_ARG;
     FusedTopk ft;
@@ -447,6 +464,7 @@ dsa_status_t dsa_sparse_mla_decode_noalloc(const uint16_t *q, const uint16_t *kv
                                            const int32_t *idx, int B, int H, int d, int r,
                                            int k, float scale, uint16_t *out, float *lse,
                                            void *stream) {
+    DSA_CALL_RANGE();
     void *scratch = nullptr;
     const dsa_status_t st = noalloc_scratch(&scratch);
     if (st != DSA_OK) return st;
@@ -462,6 +480,7 @@ dsa_status_t dsa_sparse_mla_prefill(const uint16_t *q, const uint16_t *kv_cache,
                                     int B, int T, int H, int d, int r, int k, float scale,
                                     uint16_t *out, float *lse, void *workspace,
                                     size_t workspace_bytes, void *stream) {
+    DSA_CALL_RANGE();
     return mla_common(&q, &kv_cache, 1, layout, idx, B, T, H, d, r, k, scale, &out,
                       lse ? &lse : nullptr, workspace, workspace_bytes, stream);
 }
@@ -472,6 +491,7 @@ dsa_status_t dsa_sparse_mla_shared(const uint16_t *const *q_layers,
                                    int B, int T, int H, int d, int r, int k, float scale,
                                    uint16_t *const *out_layers, float *const *lse_layers,
                                    void *workspace, size_t workspace_bytes, void *stream) {
+    DSA_CALL_RANGE();
     return mla_common(q_layers, kv_layers, n_layers, layout, idx, B, T, H, d, r, k, scale,
                       out_layers, lse_layers, workspace, workspace_bytes, stream);
 }
@@ -494,6 +514,7 @@ dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const i
                               const int32_t *pos, int n, int B, int Di, int D,
                               const dsa_cache_layout_t *layout, uint8_t *k8_cache,
                               float *k_scale, uint16_t *kv_cache, void *stream) {
+    DSA_CALL_RANGE();
     if (n < 0 || B <= 0) return DSA_ERR_INVALID_ARG;
     if (Di != 32 && Di != 64 && Di != 128) return DSA_ERR_UNSUPPORTED;
     if (n == 0) return DSA_OK;  // nothing to append (the arrays may be NULL)
@@ -521,6 +542,7 @@ dsa_status_t dsa_cache_append(const float *k_new, const uint16_t *c_new, const i
 
 dsa_status_t dsa_hisparse_init(int32_t *residency, int B, int Lmax, int32_t *slot_token,
                                uint32_t *slot_use, int C, void *stream) {
+    DSA_CALL_RANGE();
     if (!residency || !slot_token || !slot_use) return DSA_ERR_INVALID_ARG;
     if (B <= 0 || Lmax <= 0 || C <= 0) return DSA_ERR_INVALID_ARG;
     if (C > kMaxHiSlots) return DSA_ERR_UNSUPPORTED;
@@ -533,6 +555,7 @@ dsa_status_t dsa_hisparse_fetch(const int32_t *idx, int B, int k, uint32_t step,
                                 int32_t *residency, int Lmax, int32_t *slot_token,
                                 uint32_t *slot_use, int C, uint16_t *pool, int32_t *stats,
                                 void *stream) {
+    DSA_CALL_RANGE();
     if (!idx || !host_kv || !host_seq_start || !residency || !slot_token || !slot_use || !pool)
         return DSA_ERR_INVALID_ARG;
     if (B <= 0 || k <= 0 || Lmax <= 0 || C <= 0 || D <= 0 || step == 0) return DSA_ERR_INVALID_ARG;
@@ -582,6 +605,7 @@ static bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t cols, uint
 
 dsa_status_t dsa_mla_up_project(const uint16_t *latent, int64_t n, int ld, int d,
                                 const uint16_t *w, int N, uint16_t *out, void *stream) {
+    DSA_CALL_RANGE();
     if (!latent || !w || !out) return DSA_ERR_INVALID_ARG;
     if (n <= 0 || ld <= 0 || d <= 0 || N <= 0 || d > ld) return DSA_ERR_INVALID_ARG;
     if (d % 64 != 0 || N % 128 != 0 || ld % 8 != 0) return DSA_ERR_UNSUPPORTED;
@@ -606,6 +630,7 @@ dsa_status_t dsa_sparse_mha_prefill(const uint16_t *q, const uint16_t *k_up,
                                     int dn, int vd, int k, int Lmax, float scale, uint16_t *out,
                                     float *lse, void *workspace, size_t workspace_bytes,
                                     void *stream) {
+    DSA_CALL_RANGE();
     if (!q || !k_up || !v_up || !kv_cache || !layout || !idx || !q_pos || !out || !workspace)
         return DSA_ERR_INVALID_ARG;
     if (B <= 0 || T <= 0 || H <= 0 || d <= 0 || r <= 0 || dn <= 0 || vd <= 0 || k <= 0 || Lmax <= 0)
@@ -651,6 +676,7 @@ dsa_status_t dsa_sparse_mha_prefill(const uint16_t *q, const uint16_t *k_up,
 }
 
 dsa_status_t dsa_wait_probe(uint64_t *result, void *stream) {
+    DSA_CALL_RANGE();
     if (!result || (reinterpret_cast<uintptr_t>(result) & 7) != 0) return DSA_ERR_INVALID_ARG;
     return from_cuda(launch_wait_probe(reinterpret_cast<unsigned long long *>(result),
                                        static_cast<cudaStream_t>(stream)));
