@@ -115,7 +115,9 @@ dsa_status_t dsa_indexer_scores(const uint8_t *q8, const float *q_scale, const f
  *   n <= k : idx[t, :] = 0, 1, ..., n-1, then -1 up to k (the row stays dense);
  *   n >  k : the k tokens with the largest score, equal scores going to the lower token
  *            index (deterministic), listed in ascending token order.
- * Output idx [rows, k] int32.  1 <= k <= 8192.
+ * Output idx [rows, k] int32.  1 <= k <= 8192; Lmax <= 375040 (a row's scores are split
+ * over at most eight CTAs, each holding its slice in shared memory), else
+ * DSA_ERR_UNSUPPORTED before any launch.
  */
 dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int Lmax, int k,
                       int32_t *idx, void *stream);

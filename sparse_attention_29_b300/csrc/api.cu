@@ -419,7 +419,7 @@ dsa_status_t dsa_topk(const float *scores, const int32_t *q_pos, int rows, int L
     DSA_CALL_RANGE();
     if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
     if (rows <= 0 || Lmax <= 0 || k <= 0) return DSA_ERR_INVALID_ARG;
-    if (k > 8192) return DSA_ERR_UNSUPPORTED;
+    if (k > 8192 || !topk_lmax_supported(Lmax)) return DSA_ERR_UNSUPPORTED;
     TopkParams p;
     p.scores = scores;
     p.q_pos = q_pos;
@@ -451,6 +451,7 @@ dsa_status_t dsa_topk_sparse_mla_decode(const float *scores, const int32_t *q_po
     DSA_CALL_RANGE();
     if (!scores || !q_pos || !idx) return DSA_ERR_INVALID_ARG;
     if (Lmax <= 0) return DSA_ERR_INVALID_ARG;
+    if (!topk_lmax_supported(Lmax)) return DSA_ERR_UNSUPPORTED;
     FusedTopk ft;
     ft.scores = scores;
     ft.q_pos = q_pos;

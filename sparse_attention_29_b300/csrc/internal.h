@@ -124,6 +124,9 @@ struct TopkParams {
 };
 
 cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream);
+// Whether rows of Lmax scores fit the cluster top-k (the slices of a cluster of the largest
+// size in shared memory): Lmax <= 375040.
+bool topk_lmax_supported(int Lmax);
 
 // The final selection of the fused indexer + top-k: per row, from the candidates and the
 // counts the fused indexer left in cand / meta.

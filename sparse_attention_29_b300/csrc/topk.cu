@@ -309,6 +309,12 @@ static void topk_shape(const TopkParams &p, int num_sms, int &csize, int &slice_
     slice_cap = cap_of(csize);
 }
 
+bool topk_lmax_supported(int Lmax) {
+    if (Lmax <= 0) return false;
+    const int cap = (((Lmax + kMaxCluster - 1) / kMaxCluster) + 31) & ~31;
+    return topk_layout(cap).total <= 227 * 1024;
+}
+
 cudaError_t launch_topk(const TopkParams &p, int num_sms, cudaStream_t stream) {
     if (p.rows <= 0) return cudaSuccess;
     int csize, slice_cap;

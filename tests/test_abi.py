@@ -63,6 +63,9 @@ def test_null_and_range_checks_fail_before_any_launch(lib):
     # top-k: k out of range
     assert lib.dsa_topk(p, p, 4, 100, 0, p, None) == INVALID
     assert lib.dsa_topk(p, p, 4, 100, 9000, p, None) == UNSUPPORTED
+    assert lib.dsa_topk(p, p, 4, 375041, 2048, p, None) == UNSUPPORTED  # longer than a cluster holds
+    assert lib.dsa_topk_sparse_mla_decode(p, p, 375041, p, p, None, p, 4, 64, 512, 64, 2048,
+                                          0.0625, p, p, p, 0, None) == UNSUPPORTED
     assert lib.dsa_topk(None, p, 4, 100, 64, p, None) == INVALID
     # sparse MLA: shapes outside the build
     assert lib.dsa_sparse_mla_decode(p, p, ctypes.byref(L2), p, 1, 128, 512, 64, 2048,
