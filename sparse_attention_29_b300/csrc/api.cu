@@ -132,9 +132,11 @@ dsa_status_t mla_common(const uint16_t *const *q, const uint16_t *const *kv, int
     const int sms = current_sm_count();
     if (sms <= 0) return DSA_ERR_CUDA;
     const int units = B * T * n_layers;
-    // the split of a row's keys depends on the rows of one layer only, so that each layer
-    // of an IndexShare launch is computed exactly as a separate call would compute it
-    mla_split_plan(B * T, k, sms, d, &p.splits, &p.tiles_per_split);
+    // the split of a row's keys is planned for the whole launch (every layer's rows), so an
+    // IndexShare group fills the GPU as one launch: with few rows per layer its rows split
+    // less than a single layer's would (its layers' outputs then differ from separate
+    // per-layer calls by the rounding of the split merge)
+    mla_split_plan(units, k, sms, d, &p.splits, &p.tiles_per_split);
     const size_t need = mla_partial_bytes(units, p.splits, d);
     if (need) {
         if (!workspace || workspace_bytes < need) return DSA_ERR_WORKSPACE;
@@ -507,7 +509,7 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int T, int H, int d, int k, int n
     if (sms <= 0) return (size_t)-1;
     const int units = B * T * n_layers;
     int splits = 1, tps = 1;
-    mla_split_plan(B * T, k, sms, d, &splits, &tps);
+    mla_split_plan(units, k, sms, d, &splits, &tps);
     return mla_partial_bytes(units, splits, d);
 }
 
